@@ -1,0 +1,298 @@
+// HBM-bound kernels of the block: modulated RMSNorm, q/k RMSNorm + rotary pack, gated residual
+// add, SiLU gate, and the small glue of a guided denoising step (sequence assembly, guidance +
+// Euler update).  The MOSS-Image transformer page lists the first four as its hand-written kernels
+// ("modulated RMSNorm, q/k norm and rotary into packed rows, situ [SiLU gate], gated add").
+//
+// All of them move 16-byte vectors (8 bf16) per thread, reduce in fp32 with a fixed shuffle
+// order (so results repeat bit for bit), and round once to bf16 at the output.
+#include "mi_internal.h"
+#include "ptx.cuh"
+
+namespace mi {
+
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+  f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+// ------------------------------------------------------------------------------------ adaLN norm
+// out[i] = x[in_row(i)] * rsqrt(mean(x^2) + eps) * (1 + scale[b]) + shift[b]; one warp per row.
+// Row i of the output reads input row (i / out_seq) * in_seq + in_off + i % out_seq, which lets
+// the final norm of a denoising step read only the image rows of each batch element.
+constexpr int kNormMaxVec = 16;  // hidden <= 16 * 256 = 4096
+
+__global__ void __launch_bounds__(256) mod_rmsnorm_kernel(const __nv_bfloat16* __restrict__ x,
+                                                          const __nv_bfloat16* __restrict__ shift,
+                                                          const __nv_bfloat16* __restrict__ scale, int mod_bstride,
+                                                          __nv_bfloat16* __restrict__ out, int rows, int out_seq,
+                                                          int in_seq, int in_off, int hidden, float eps) {
+  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp_global >= rows) return;
+  const int b = warp_global / out_seq;
+  const int in_row = b * in_seq + in_off + warp_global % out_seq;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)in_row * hidden);
+  const int nv = hidden >> 8;  // 16-byte vectors per lane
+  uint4 v[kNormMaxVec];
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kNormMaxVec; ++i) {
+    if (i < nv) {
+      v[i] = xr[i * 32 + lane];
+      float f[8];
+      unpack8(v[i], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float rstd = rsqrtf(ss / (float)hidden + eps);
+  const uint4* sh = reinterpret_cast<const uint4*>(shift + (size_t)b * mod_bstride);
+  const uint4* sc = reinterpret_cast<const uint4*>(scale + (size_t)b * mod_bstride);
+  uint4* orow = reinterpret_cast<uint4*>(out + (size_t)warp_global * hidden);
+#pragma unroll
+  for (int i = 0; i < kNormMaxVec; ++i) {
+    if (i < nv) {
+      float f[8], fs[8], fc[8];
+      unpack8(v[i], f);
+      unpack8(__ldg(sh + i * 32 + lane), fs);
+      unpack8(__ldg(sc + i * 32 + lane), fc);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = fmaf(f[e] * rstd, 1.0f + fc[e], fs[e]);
+      orow[i * 32 + lane] = pack8(f);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------ q/k pack
+// One warp per (row, head): lanes 0-15 take q, lanes 16-31 take k, 8 consecutive elements each
+// (4 rotary pairs).  RMSNorm over the 128 elements of the head, gain, then the rotation of the
+// interleaved pairs (2p, 2p+1) by the table angle at (row, p).  Output rows are packed per head:
+// qp/kp[(b * heads + h) * S + s][0..128).
+__global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __nv_bfloat16* __restrict__ qkv,
+                                                           const __nv_bfloat16* __restrict__ wq,
+                                                           const __nv_bfloat16* __restrict__ wk,
+                                                           const float* __restrict__ cosv,
+                                                           const float* __restrict__ sinv, int rope_bstride,
+                                                           __nv_bfloat16* __restrict__ qp,
+                                                           __nv_bfloat16* __restrict__ kp, int batch, int seq,
+                                                           int heads, float eps) {
+  const long long item = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long total = (long long)batch * seq * heads;
+  if (item >= total) return;
+  const int h = (int)(item % heads);
+  const long long row = item / heads;  // b * seq + s
+  const int b = (int)(row / seq);
+  const int s = (int)(row % seq);
+  const int H = heads * kHeadDim;
+  const int which = lane >> 4;  // 0: q, 1: k
+  const int sub = lane & 15;
+  const int e0 = sub * 8;
+  const uint4 v = *reinterpret_cast<const uint4*>(qkv + (size_t)row * 3 * H + (size_t)which * H +
+                                                  (size_t)h * kHeadDim + e0);
+  float f[8];
+  unpack8(v, f);
+  float ss = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float rstd = rsqrtf(ss * (1.0f / kHeadDim) + eps);
+  float g[8];
+  unpack8(__ldg(reinterpret_cast<const uint4*>((which ? wk : wq) + e0)), g);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) f[e] = f[e] * rstd * g[e];
+  const float* cr = cosv + (size_t)b * rope_bstride + (size_t)s * (kHeadDim / 2) + sub * 4;
+  const float* sr = sinv + (size_t)b * rope_bstride + (size_t)s * (kHeadDim / 2) + sub * 4;
+  const float4 c4 = __ldg(reinterpret_cast<const float4*>(cr));
+  const float4 s4 = __ldg(reinterpret_cast<const float4*>(sr));
+  const float cs[4] = {c4.x, c4.y, c4.z, c4.w};
+  const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
+  float o[8];
+#pragma unroll
+  for (int pr = 0; pr < 4; ++pr) {
+    const float a = f[2 * pr], bb = f[2 * pr + 1];
+    o[2 * pr] = fmaf(a, cs[pr], -bb * sn[pr]);
+    o[2 * pr + 1] = fmaf(a, sn[pr], bb * cs[pr]);
+  }
+  __nv_bfloat16* dst = (which ? kp : qp) + (((size_t)b * heads + h) * seq + s) * kHeadDim + e0;
+  *reinterpret_cast<uint4*>(dst) = pack8(o);
+}
+
+// ------------------------------------------------------------------------------------ gated add
+// out = x + gate[b] * y (fp32 fma, one rounding); the same expression as the fused GEMM epilogue.
+__global__ void __launch_bounds__(256) gated_add_kernel(const __nv_bfloat16* __restrict__ x,
+                                                        const __nv_bfloat16* __restrict__ y,
+                                                        const __nv_bfloat16* __restrict__ gate, int gate_bstride,
+                                                        __nv_bfloat16* __restrict__ out, long long n_vec, int seq,
+                                                        int hidden) {
+  const int vpr = hidden >> 3;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / vpr;
+    const int cv = (int)(i % vpr);
+    const int b = (int)(row / seq);
+    float fx[8], fy[8], fg[8];
+    unpack8(reinterpret_cast<const uint4*>(x)[i], fx);
+    unpack8(reinterpret_cast<const uint4*>(y)[i], fy);
+    unpack8(__ldg(reinterpret_cast<const uint4*>(gate + (size_t)b * gate_bstride) + cv), fg);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) fx[e] = fmaf(fg[e], fy[e], fx[e]);
+    reinterpret_cast<uint4*>(out)[i] = pack8(fx);
+  }
+}
+
+// ------------------------------------------------------------------------------------ SiLU gate
+// m[r, j] = silu(gu[r, j]) * gu[r, I + j]; the same expression as the fused GEMM epilogue.
+__global__ void __launch_bounds__(256) silu_gate_kernel(const __nv_bfloat16* __restrict__ gu,
+                                                        __nv_bfloat16* __restrict__ m, long long n_vec, int inter) {
+  const int vpr = inter >> 3;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / vpr;
+    const int cv = (int)(i % vpr);
+    const uint4* src = reinterpret_cast<const uint4*>(gu + (size_t)row * 2 * inter);
+    float g[8], u[8];
+    unpack8(src[cv], g);
+    unpack8(src[vpr + cv], u);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) g[e] = silu_f(g[e]) * u[e];
+    reinterpret_cast<uint4*>(m)[i] = pack8(g);
+  }
+}
+
+// ------------------------------------------------------------------------------------ step glue
+// x[b, t] = text[b, t] for t < T, x[b, T + n] = u[n] (the embedded latent is shared by the batch).
+__global__ void __launch_bounds__(256) assemble_seq_kernel(const uint4* __restrict__ text, const uint4* __restrict__ u,
+                                                           uint4* __restrict__ x, int batch, int text_pad,
+                                                           int n_img, int vpr) {
+  const long long S = text_pad + n_img;
+  const long long total = (long long)batch * S * vpr;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / vpr;
+    const int cv = (int)(i % vpr);
+    const int b = (int)(row / S);
+    const int s = (int)(row % S);
+    x[i] = s < text_pad ? text[((long long)b * text_pad + s) * vpr + cv] : u[(long long)(s - text_pad) * vpr + cv];
+  }
+}
+
+__global__ void __launch_bounds__(256) copy_vec_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                       long long n_vec) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec;
+       i += (long long)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
+// v = v_neg + g (v_pos - v_neg) in fp32, latent <- bf16(latent + dt v).  vel is [2, N, C].
+__global__ void __launch_bounds__(256) cfg_euler_kernel(const __nv_bfloat16* __restrict__ vel,
+                                                        __nv_bfloat16* __restrict__ latent, long long n, float dt,
+                                                        float guidance, int batch) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float vp = __bfloat162float(vel[i]);
+    const float v = batch > 1 ? fmaf(guidance, vp - __bfloat162float(vel[n + i]), __bfloat162float(vel[n + i])) : vp;
+    latent[i] = __float2bfloat16_rn(fmaf(dt, v, __bfloat162float(latent[i])));
+  }
+}
+
+int grid_for(long long work_items, int threads) {
+  long long g = (work_items + threads - 1) / threads;
+  const long long cap = 152LL * 16;  // enough resident blocks for a grid-stride loop
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return (int)g;
+}
+
+}  // namespace
+
+cudaError_t mod_rmsnorm_launch(const __nv_bfloat16* x, const __nv_bfloat16* shift, const __nv_bfloat16* scale,
+                               int mod_bstride, __nv_bfloat16* out, int rows, int seq, int hidden, float eps,
+                               cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = (rows * 32 + threads - 1) / threads;
+  mod_rmsnorm_kernel<<<blocks, threads, 0, s>>>(x, shift, scale, mod_bstride, out, rows, seq, seq, 0, hidden, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t mod_rmsnorm_rows_launch(const __nv_bfloat16* x, const __nv_bfloat16* shift, const __nv_bfloat16* scale,
+                                    int mod_bstride, __nv_bfloat16* out, int rows, int out_seq, int in_seq, int in_off,
+                                    int hidden, float eps, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = (rows * 32 + threads - 1) / threads;
+  mod_rmsnorm_kernel<<<blocks, threads, 0, s>>>(x, shift, scale, mod_bstride, out, rows, out_seq, in_seq, in_off,
+                                                hidden, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t qk_norm_rope_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* wq, const __nv_bfloat16* wk,
+                                const float* cos, const float* sin, int rope_bstride, __nv_bfloat16* qp,
+                                __nv_bfloat16* kp, int batch, int seq, int n_heads, float eps, cudaStream_t s) {
+  const long long warps = (long long)batch * seq * n_heads;
+  if (warps <= 0) return cudaSuccess;
+  const int threads = 256;
+  const long long blocks = (warps * 32 + threads - 1) / threads;
+  qk_norm_rope_kernel<<<(unsigned)blocks, threads, 0, s>>>(qkv, wq, wk, cos, sin, rope_bstride, qp, kp, batch, seq,
+                                                           n_heads, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t gated_add_launch(const __nv_bfloat16* x, const __nv_bfloat16* y, const __nv_bfloat16* gate,
+                             int gate_bstride, __nv_bfloat16* out, int rows, int seq, int hidden, cudaStream_t s) {
+  const long long n_vec = (long long)rows * hidden / 8;
+  if (n_vec <= 0) return cudaSuccess;
+  gated_add_kernel<<<grid_for(n_vec, 256), 256, 0, s>>>(x, y, gate, gate_bstride, out, n_vec, seq, hidden);
+  return cudaGetLastError();
+}
+
+cudaError_t silu_gate_launch(const __nv_bfloat16* gu, __nv_bfloat16* m, int rows, int inter, cudaStream_t s) {
+  const long long n_vec = (long long)rows * inter / 8;
+  if (n_vec <= 0) return cudaSuccess;
+  silu_gate_kernel<<<grid_for(n_vec, 256), 256, 0, s>>>(gu, m, n_vec, inter);
+  return cudaGetLastError();
+}
+
+cudaError_t assemble_seq_launch(const __nv_bfloat16* text, const __nv_bfloat16* u, __nv_bfloat16* x, int batch,
+                                int text_pad, int n_img, int hidden, cudaStream_t s) {
+  const int vpr = hidden / 8;
+  const long long total = (long long)batch * (text_pad + n_img) * vpr;
+  if (total <= 0) return cudaSuccess;
+  assemble_seq_kernel<<<grid_for(total, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(text),
+                                                            reinterpret_cast<const uint4*>(u),
+                                                            reinterpret_cast<uint4*>(x), batch, text_pad, n_img, vpr);
+  return cudaGetLastError();
+}
+
+cudaError_t copy_rows_launch(const __nv_bfloat16* src, __nv_bfloat16* dst, size_t n_elems, cudaStream_t s) {
+  const long long n_vec = (long long)(n_elems / 8);
+  if (n_vec <= 0) return cudaSuccess;
+  copy_vec_kernel<<<grid_for(n_vec, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(src),
+                                                        reinterpret_cast<uint4*>(dst), n_vec);
+  return cudaGetLastError();
+}
+
+cudaError_t cfg_euler_launch(const __nv_bfloat16* vel, __nv_bfloat16* latent, int n_img, int channels, float dt,
+                             float guidance, int batch, cudaStream_t s) {
+  const long long n = (long long)n_img * channels;
+  if (n <= 0) return cudaSuccess;
+  cfg_euler_kernel<<<grid_for(n, 256), 256, 0, s>>>(vel, latent, n, dt, guidance, batch);
+  return cudaGetLastError();
+}
+
+}  // namespace mi

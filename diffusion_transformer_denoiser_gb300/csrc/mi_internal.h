@@ -1,0 +1,75 @@
+// Internal declarations shared by the launch layer and the kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mi {
+
+constexpr int kMaxDevices = 64;
+constexpr int kHeadDim = 128;
+
+enum GemmEpilogue : int {
+  EPI_STORE = 0,           // C = A W^T
+  EPI_GATED_RESIDUAL = 1,  // C = resid + gate[b] * bf16(A W^T)
+  EPI_SILU_GATE = 2,       // C[:, j] = silu(bf16(A Wg^T)[:, j]) * bf16(A Wu^T)[:, j], W = [Wg; Wu]
+};
+
+struct GemmArgs {
+  int M, N, K;              // for EPI_SILU_GATE, N is the width of the output (I), W has 2N rows
+  __nv_bfloat16* C;
+  int ldc;
+  const __nv_bfloat16* resid;  // EPI_GATED_RESIDUAL: [M, ldr]
+  int ldr;
+  const __nv_bfloat16* gate;   // EPI_GATED_RESIDUAL: gate of batch b at gate + b * gate_bstride
+  int gate_bstride;
+  int seq;                     // rows per batch element (selects the gate vector)
+  int* err;                    // device error flag
+};
+
+cudaError_t gemm_launch(int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int num_sms,
+                        cudaStream_t s);
+
+struct AttnArgs {
+  int batch, seq, n_heads;
+  const uint8_t* key_mask;     // [B, S] or null
+  __nv_bfloat16* out;          // [B, S, n_heads * 128]
+  float scale_log2;            // log2(e) / sqrt(128)
+  int* err;
+};
+
+// q/k maps: 3-D over (128, S, B * n_heads); v map: 4-D over (128, n_heads, S, B) of the qkv buffer.
+cudaError_t attention_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const AttnArgs& a, cudaStream_t s);
+
+// Element-wise kernels (elementwise.cu).
+cudaError_t mod_rmsnorm_launch(const __nv_bfloat16* x, const __nv_bfloat16* shift, const __nv_bfloat16* scale,
+                               int mod_bstride, __nv_bfloat16* out, int rows, int seq, int hidden, float eps,
+                               cudaStream_t s);
+cudaError_t qk_norm_rope_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* wq, const __nv_bfloat16* wk,
+                                const float* cos, const float* sin, int rope_bstride, __nv_bfloat16* qp,
+                                __nv_bfloat16* kp, int batch, int seq, int n_heads, float eps, cudaStream_t s);
+cudaError_t gated_add_launch(const __nv_bfloat16* x, const __nv_bfloat16* y, const __nv_bfloat16* gate,
+                             int gate_bstride, __nv_bfloat16* out, int rows, int seq, int hidden, cudaStream_t s);
+cudaError_t silu_gate_launch(const __nv_bfloat16* gu, __nv_bfloat16* m, int rows, int inter, cudaStream_t s);
+cudaError_t assemble_seq_launch(const __nv_bfloat16* text, const __nv_bfloat16* u, __nv_bfloat16* x, int batch,
+                                int text_pad, int n_img, int hidden, cudaStream_t s);
+cudaError_t mod_rmsnorm_rows_launch(const __nv_bfloat16* x, const __nv_bfloat16* shift, const __nv_bfloat16* scale,
+                                    int mod_bstride, __nv_bfloat16* out, int rows, int out_seq, int in_seq, int in_off,
+                                    int hidden, float eps, cudaStream_t s);
+cudaError_t copy_rows_launch(const __nv_bfloat16* src, __nv_bfloat16* dst, size_t n_elems, cudaStream_t s);
+cudaError_t cfg_euler_launch(const __nv_bfloat16* vel, __nv_bfloat16* latent, int n_img, int channels, float dt,
+                             float guidance, int batch, cudaStream_t s);
+
+// Tensor maps (tmap.cpp).
+bool encode_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
+                    uint32_t box_inner, uint32_t box_rows);
+bool encode_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
+                    uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
+bool encode_4d_bf16(CUtensorMap* m, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
+                    const uint32_t box[4]);
+
+}  // namespace mi

@@ -1,0 +1,218 @@
+/*
+ * mi_block: forward pass of a MOSS-Image-style diffusion-transformer (DiT) block on one GB300
+ * (sm_103a), plus one guided denoising step built from it.
+ *
+ * What the block computes is named on the TensorFold page "MOSS-Image transformer on CUDA"
+ * (PR #1528): section "What it adds" lists the hand-written kernels (modulated RMSNorm, q/k norm
+ * and rotary into packed rows, the SiLU gate, gated add), the bf16 projections with fp32 sums and
+ * the full head-128 attention; its precision bullet fixes bf16 weights and activations with fp32
+ * sums, norms and softmax.  The guided step (empty negative prompt, guidance, Euler schedule) is
+ * the host loop of PR #2281, section "What this changes".  Where the pages name an operation
+ * without its formula, the plain definition is used:
+ *
+ *   h   = x * rsqrt(mean(x^2) + eps) * (1 + scale1) + shift1
+ *   qkv = h W_qkv^T;  q, k per head: RMSNorm over 128 with gain, then rotary on pairs (2p, 2p+1)
+ *   o   = softmax(q k^T / sqrt(128) with masked keys at -inf) v
+ *   x1  = x + gate1 * (o W_o^T)
+ *   h2  = x1 * rsqrt(mean(x1^2) + eps) * (1 + scale2) + shift2
+ *   m   = silu(h2 Wg^T) * (h2 Wu^T),  W_gu = [Wg; Wu]
+ *   y   = x1 + gate2 * (m W_d^T)
+ *
+ * Conventions of every entry point:
+ *   - All tensors are device pointers owned by the caller; every bf16 tensor is row-major,
+ *     16-byte aligned, and passed as `void*` holding __nv_bfloat16 values.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is only enqueued:
+ *     nothing here synchronises, allocates device memory on the forward path, prints or aborts.
+ *   - Every function returns mi_status; on failure mi_last_error() (thread-local) says why and
+ *     nothing was enqueued.
+ *   - Results are deterministic: the same inputs on the same GPU and build give the same bytes.
+ */
+#ifndef MI_BLOCK_H
+#define MI_BLOCK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MI_ABI_VERSION 1
+
+typedef enum mi_status {
+  MI_OK = 0,
+  MI_ERR_INVALID_ARG = 1,  /* null pointer, misaligned pointer, bad geometry */
+  MI_ERR_UNSUPPORTED = 2,  /* device is not sm_103, head_dim != 128, or a shape the kernels refuse */
+  MI_ERR_WORKSPACE = 3,    /* workspace pointer null/misaligned or smaller than the query says */
+  MI_ERR_CUDA = 4,         /* a CUDA runtime call failed (message carries the CUDA error string) */
+  MI_ERR_DEVICE = 5        /* a kernel reported a pipeline timeout through the device error flag */
+} mi_status;
+
+/* Thread-local message of the last failed call on this thread ("" if none). */
+const char* mi_last_error(void);
+
+/* MI_ABI_VERSION of the loaded library. */
+int mi_abi_version(void);
+
+/* MI_OK if the current device is an sm_103 GPU the kernels were built for. */
+mi_status mi_device_supported(void);
+
+/* Reads and clears the device error flag of the current device.  *code = 0 when every kernel
+ * since the last call finished its pipeline; otherwise the first timeout code recorded (a kernel
+ * whose wait exceeded its wall-clock limit returns early and leaves its outputs undefined).
+ * Synchronises the device (diagnostic call, not for the hot path). */
+mi_status mi_device_error(int* code);
+
+/* ---------------------------------------------------------------------------------- block --- */
+
+typedef struct mi_block_desc {
+  int hidden;      /* H: multiple of 256, at most 4096; H = n_heads * head_dim */
+  int n_heads;
+  int head_dim;    /* must be 128 */
+  int mlp_inter;   /* I: multiple of 128 */
+  float eps;       /* RMSNorm epsilon of all three norms (1e-6 in the synthetic workloads) */
+  int fuse_epilogues; /* 1: SiLU gate fused into the gate/up GEMM and the gated residual adds into
+                         the W_o / W_d GEMMs; 0: separate kernels.  Both give identical bytes. */
+  /* Weights (bf16, device, read-only, must outlive the mi_block): */
+  const void* w_qkv;    /* [3H, H]: rows [0,H) q, [H,2H) k, [2H,3H) v; head j = rows 128j.. of each */
+  const void* w_o;      /* [H, H] */
+  const void* w_gu;     /* [2I, H]: rows [0,I) gate, [I,2I) up */
+  const void* w_d;      /* [H, I] */
+  const void* q_norm_w; /* [128]: gain of the per-head q RMSNorm, shared by all heads */
+  const void* k_norm_w; /* [128] */
+} mi_block_desc;
+
+/* Sequence layout of one batch element: text_pad prompt rows, then grid_h * grid_w image tokens
+ * in row-major (r, c) order.  S = text_pad + grid_h * grid_w rows per element. */
+typedef struct mi_seq_layout {
+  int batch;
+  int text_pad;
+  int grid_h;
+  int grid_w;
+} mi_seq_layout;
+
+typedef struct mi_block mi_block;
+
+/* Validates the geometry, the weight pointers and the device (sm_103 required, else
+ * MI_ERR_UNSUPPORTED) and builds the TMA descriptors of the weights.  Refuses any null weight. */
+mi_status mi_block_init(mi_block** out, const mi_block_desc* desc);
+void mi_block_destroy(mi_block* blk);
+
+/* Workspace bytes mi_block_forward needs for `batch` elements of `seq` rows. */
+mi_status mi_block_workspace_size(const mi_block* blk, int batch, int seq, size_t* bytes);
+
+/* Intermediates left in the workspace by the last forward (for parity checks). */
+typedef enum mi_tensor {
+  MI_T_H = 0,   /* [B*S, H]  modulated RMSNorm #1 */
+  MI_T_QKV = 1, /* [B*S, 3H] QKV projection */
+  MI_T_QP = 2,  /* [B, heads, S, 128] q after norm + rotary */
+  MI_T_KP = 3,  /* [B, heads, S, 128] k after norm + rotary */
+  MI_T_O = 4,   /* [B*S, H]  attention output, heads concatenated */
+  MI_T_A = 5,   /* [B*S, H]  o W_o^T               (only when epilogues are not fused) */
+  MI_T_X1 = 6,  /* [B*S, H]  first residual */
+  MI_T_H2 = 7,  /* [B*S, H]  modulated RMSNorm #2 */
+  MI_T_GU = 8,  /* [B*S, 2I] gate/up projection    (only when epilogues are not fused) */
+  MI_T_M = 9,   /* [B*S, I]  SiLU gate */
+  MI_T_DN = 10  /* [B*S, H]  down projection       (only when epilogues are not fused) */
+} mi_tensor;
+
+/* Byte offset and size of intermediate `which` inside the workspace; MI_ERR_UNSUPPORTED when the
+ * block's fusion setting does not materialise it. */
+mi_status mi_block_tensor_offset(const mi_block* blk, int batch, int seq, int which, size_t* offset,
+                                 size_t* bytes);
+
+/*
+ * One block forward over L->batch elements.
+ *   x        bf16 [B, S, H] input rows (text rows then image tokens)
+ *   y        bf16 [B, S, H] output; y == x (in place) is allowed, any other overlap is not
+ *   mod      bf16 [B, 6, H]: shift1, scale1, gate1, shift2, scale2, gate2 for batch element b,
+ *            applied to every row of that element
+ *   rope_cos, rope_sin  fp32 [S, 64] angle tables (element b reads base + b * rope_bstride;
+ *            rope_bstride = 0 shares one table); pair p of row s rotates by the angle at [s, p]
+ *   key_mask uint8 [B, S]: 0 excludes the key row from attention (padded prompt rows), or NULL.
+ *            A query row whose keys are all masked gets a zero attention output.
+ *   ws       device workspace of at least mi_block_workspace_size bytes, 1024-byte aligned
+ */
+mi_status mi_block_forward(mi_block* blk, const mi_seq_layout* L, const void* x, void* y, const void* mod,
+                           const float* rope_cos, const float* rope_sin, int rope_bstride,
+                           const uint8_t* key_mask, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------- denoising step --- */
+
+typedef struct mi_model_desc {
+  int n_blocks;
+  const mi_block_desc* blocks; /* n_blocks descriptors (same geometry) */
+  int latent_ch;               /* C: latent channels, multiple of 64 */
+  const void* w_in;            /* bf16 [H, C]: latent -> hidden embedding */
+  const void* w_out;           /* bf16 [C, H]: hidden -> velocity projection */
+} mi_model_desc;
+
+typedef struct mi_model mi_model;
+
+mi_status mi_model_init(mi_model** out, const mi_model_desc* desc);
+void mi_model_destroy(mi_model* model);
+mi_status mi_model_workspace_size(const mi_model* model, const mi_seq_layout* L, size_t* bytes);
+
+/*
+ * One guided denoising step (PR #2281 "What this changes": the pipeline's schedule and
+ * classifier-free guidance with an empty negative prompt; PR #1528 "Measured": Euler steps):
+ *   u = latent W_in^T;  x_b = [text_rows_b ; u];  x_b <- every block;
+ *   vel_b = (RMSNorm(image rows of x_b) (1 + scale_f) + shift_f) W_out^T;
+ *   v = vel_1 + guidance (vel_0 - vel_1) when batch == 2 (element 0 the prompt, 1 the negative),
+ *   v = vel_0 when batch == 1;  latent <- latent + dt v.
+ *   latent    bf16 [N, C] (N = grid_h * grid_w), updated in place
+ *   text_rows bf16 [B, T, H]
+ *   mods      bf16 [n_blocks, B, 6, H] (per block, as in mi_block_forward)
+ *   mod_final bf16 [B, 2, H]: shift_f, scale_f
+ *   skip_neg  uint8 [n_blocks] or NULL: a nonzero entry makes the negative element bypass that block
+ */
+mi_status mi_denoise_step(mi_model* model, const mi_seq_layout* L, void* latent, const void* text_rows,
+                          const void* mods, const void* mod_final, const float* rope_cos, const float* rope_sin,
+                          int rope_bstride, const uint8_t* key_mask, float dt, float guidance,
+                          const uint8_t* skip_neg, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ single kernels --- */
+/* The steps of the block as separate calls (same kernels mi_block_forward launches). */
+
+/* out[r] = x[r] * rsqrt(mean(x[r]^2) + eps) * (1 + mod[b, scale_row]) + mod[b, shift_row],
+ * b = r / seq; x, out [batch * seq, hidden]; mod [batch, 6, hidden]. */
+mi_status mi_mod_rmsnorm(const void* x, const void* mod, int shift_row, int scale_row, void* out, int batch,
+                         int seq, int hidden, float eps, void* stream);
+
+/* c[m, n] = sum_k a[m, k] w[n, k] (fp32 sums, bf16 out).  a [m, k], w [n, k], c [m, n];
+ * k a multiple of 64, n a multiple of 8. */
+mi_status mi_gemm_bf16(const void* a, const void* w, void* c, int m, int n, int k, void* stream);
+
+/* out = resid + mod[b, gate_row] * bf16(a w^T), b = row / seq (the W_o / W_d projections fused
+ * with the gated residual).  resid, out [m, n] (out may equal resid). */
+mi_status mi_gemm_bf16_gated_residual(const void* a, const void* w, const void* resid, const void* mod,
+                                      int gate_row, void* out, int m, int n, int k, int seq, void* stream);
+
+/* m_out[:, j] = silu(bf16(a wg^T)[:, j]) * bf16(a wu^T)[:, j] with w = [wg; wu] of 2*inter rows
+ * (the gate/up projection fused with the SiLU gate).  inter a multiple of 128. */
+mi_status mi_gemm_bf16_silu_gate(const void* a, const void* w, void* m_out, int m, int inter, int k,
+                                 void* stream);
+
+/* Per-head RMSNorm (gains q_norm_w / k_norm_w [128]) and rotary of the q and k columns of
+ * qkv [batch * seq, 3H], written to qp, kp [batch, heads, seq, 128]. */
+mi_status mi_qk_norm_rope(const void* qkv, const void* q_norm_w, const void* k_norm_w, const float* rope_cos,
+                          const float* rope_sin, int rope_bstride, void* qp, void* kp, int batch, int seq,
+                          int n_heads, float eps, void* stream);
+
+/* o [batch * seq, heads * 128] = softmax(q k^T / sqrt(128)) v per (batch, head); q = qp, k = kp
+ * as written by mi_qk_norm_rope, v read from columns [2H, 3H) of qkv; key_mask as above. */
+mi_status mi_attention(const void* qp, const void* kp, const void* qkv, const uint8_t* key_mask, void* o,
+                       int batch, int seq, int n_heads, void* stream);
+
+/* out = x + mod[b, gate_row] * y, b = row / seq; x, y, out [batch * seq, hidden]. */
+mi_status mi_gated_add(const void* x, const void* y, const void* mod, int gate_row, void* out, int batch,
+                       int seq, int hidden, void* stream);
+
+/* m[r, j] = silu(gu[r, j]) * gu[r, inter + j]; gu [rows, 2 * inter], m [rows, inter]. */
+mi_status mi_silu_gate(const void* gu, void* m, int rows, int inter, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MI_BLOCK_H */

@@ -167,6 +167,19 @@ def silu_gate(gu: np.ndarray, inter: int) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------------------------
+# projections (PR #1528: bf16 GEMMs with fp32 sums; here exact in float64)
+# ----------------------------------------------------------------------------------------------
+def project(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """x W^T for rows x [..., K] and a weight W [N, K] (no bias)."""
+    return x @ w.T
+
+
+def gated_residual(x, gate, y):
+    """x + gate * y (gate broadcast over rows)."""
+    return x + gate * y
+
+
+# ----------------------------------------------------------------------------------------------
 # the block (the step list of PR #1528's kernels, with projections between them)
 # ----------------------------------------------------------------------------------------------
 def block_forward(x, mod, w_qkv, w_o, w_gu, w_d, q_norm_w, k_norm_w, rope_cos, rope_sin,
@@ -186,26 +199,53 @@ def block_forward(x, mod, w_qkv, w_o, w_gu, w_d, q_norm_w, k_norm_w, rope_cos, r
         shift1, scale1, gate1, shift2, scale2, gate2 = mod[b]
         xb = x[b]
         h = modulated_rms_norm(xb, shift1, scale1, eps)                      # step 1
-        qkv = h @ w_qkv.T                                                     # step 2
+        qkv = project(h, w_qkv)                                               # step 2
         q, k, v = qkv[:, :H], qkv[:, H:2 * H], qkv[:, 2 * H:]
         qn = rope(head_rms_norm(q, q_norm_w, nh, eps), rope_cos, rope_sin)   # steps 3-4
         kn = rope(head_rms_norm(k, k_norm_w, nh, eps), rope_cos, rope_sin)
         vh = v.reshape(S, nh, d)
         valid = None if key_mask is None else np.asarray(key_mask[b]) != 0
         o = attention(qn, kn, vh, valid).reshape(S, H)                       # step 5
-        a = o @ w_o.T
-        x1 = xb + gate1 * a                                                   # step 6
+        a = project(o, w_o)
+        x1 = gated_residual(xb, gate1, a)                                     # step 6
         h2 = modulated_rms_norm(x1, shift2, scale2, eps)                     # step 7
-        gu = h2 @ w_gu.T
+        gu = project(h2, w_gu)
         m = silu_gate(gu, I)                                                  # step 8
-        dn = m @ w_d.T
-        y = x1 + gate2 * dn                                                   # step 9
+        dn = project(m, w_d)
+        y = gated_residual(x1, gate2, dn)                                     # step 9
         for name, val in (("h", h), ("qkv", qkv), ("q", qn.transpose(1, 0, 2)),
                           ("k", kn.transpose(1, 0, 2)), ("v", vh.transpose(1, 0, 2)), ("o", o),
                           ("a", a), ("x1", x1), ("h2", h2), ("gu", gu), ("m", m), ("dn", dn),
                           ("y", y)):
             outs[name].append(val)
     return {k: np.stack(v) for k, v in outs.items()}
+
+
+def block_forward_rows(x, mod, w_qkv, w_o, w_gu, w_d, q_norm_w, k_norm_w, rope_cos, rope_sin, rows,
+                       key_mask=None, n_heads=None, eps=EPS_DEFAULT) -> np.ndarray:
+    """The block output y for the query rows `rows` of batch element 0 only ([len(rows), H]).
+
+    Same step list as block_forward; keys and values are still formed from every row (attention
+    reads all of them), but the query-side steps run for the selected rows alone.  Used to time
+    the oracle on a bounded sample of a large workload."""
+    S, H = x.shape[1], x.shape[2]
+    d = q_norm_w.shape[0]
+    nh = n_heads if n_heads is not None else H // d
+    inter = w_d.shape[1]
+    shift1, scale1, gate1, shift2, scale2, gate2 = mod[0]
+    xb = x[0]
+    h = modulated_rms_norm(xb, shift1, scale1, eps)
+    k = project(h, w_qkv[H:2 * H])
+    v = project(h, w_qkv[2 * H:])
+    q = project(h[rows], w_qkv[:H])
+    qn = rope(head_rms_norm(q, q_norm_w, nh, eps), rope_cos[rows], rope_sin[rows])
+    kn = rope(head_rms_norm(k, k_norm_w, nh, eps), rope_cos, rope_sin)
+    valid = None if key_mask is None else np.asarray(key_mask[0]) != 0
+    o = attention(qn, kn, v.reshape(S, nh, d), valid).reshape(len(rows), H)
+    x1 = gated_residual(xb[rows], gate1, project(o, w_o))
+    h2 = modulated_rms_norm(x1, shift2, scale2, eps)
+    m = silu_gate(project(h2, w_gu), inter)
+    return gated_residual(x1, gate2, project(m, w_d))
 
 
 def block_forward_inputs(inp, eps=None) -> Dict[str, np.ndarray]:

@@ -1,0 +1,55 @@
+"""Shared helpers of the GPU parity tests: bf16 bits <-> torch tensors, and the parity bar."""
+import numpy as np
+import pytest
+import torch
+
+COS_MIN = 0.9995        # cosine similarity against the float64 oracle, per output tensor
+REL_MAX = 3e-2          # max |gpu - oracle| <= REL_MAX * max |oracle|, per output tensor
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def to_dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev())
+
+
+def to_dev(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+
+
+def bf16_to_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def parity_stats(got: np.ndarray, ref: np.ndarray):
+    g = np.asarray(got, dtype=np.float64).ravel()
+    r = np.asarray(ref, dtype=np.float64).ravel()
+    denom = np.sqrt((g * g).sum() * (r * r).sum())
+    cos = float((g * r).sum() / denom) if denom > 0 else (1.0 if np.array_equal(g, r) else 0.0)
+    mref = float(np.abs(r).max()) if r.size else 0.0
+    err = float(np.abs(g - r).max()) if r.size else 0.0
+    return cos, err, mref
+
+
+def assert_parity(got, ref, name=""):
+    cos, err, mref = parity_stats(got, ref)
+    assert np.isfinite(got).all(), f"{name}: non-finite GPU output"
+    assert cos >= COS_MIN, f"{name}: cosine {cos:.6f} < {COS_MIN}"
+    assert err <= REL_MAX * mref + 1e-30, f"{name}: max|err| {err:.4g} > {REL_MAX} * max|ref| {mref:.4g}"
+    return cos, err / mref if mref > 0 else 0.0
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import diffusion_transformer_denoiser_gb300 as mi
+    mi.lib()
+    if not mi.device_supported():
+        pytest.fail("device is not sm_103: " + mi.lib().mi_last_error().decode())
+    return mi

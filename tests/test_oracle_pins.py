@@ -528,3 +528,16 @@ def test_planted_mistake_is_caught(monkeypatch, name, mutant, pins):
     for pin in pins:
         with pytest.raises(AssertionError):
             pin()
+
+
+def test_row_subset_forward_matches_full_forward():
+    g = mi_synth.GEOMETRIES["small_ragged_17x19"]
+    inp = mi_synth.block_inputs(g, 7)
+    full = O.block_forward_inputs(inp)["y"][0]
+    w = inp.weights
+    rows = np.array([0, 5, 12, 13, 200, g.seq - 1])
+    sub = O.block_forward_rows(O.widen(inp.x), O.widen(inp.mod), O.widen(w.w_qkv), O.widen(w.w_o),
+                               O.widen(w.w_gu), O.widen(w.w_d), O.widen(w.q_norm_w), O.widen(w.k_norm_w),
+                               inp.rope_cos.astype(np.float64), inp.rope_sin.astype(np.float64), rows,
+                               inp.key_mask, g.n_heads)
+    np.testing.assert_allclose(sub, full[rows], rtol=0, atol=1e-12)
