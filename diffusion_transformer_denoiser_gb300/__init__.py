@@ -227,10 +227,15 @@ class Model:
 
     def denoise_step(self, layout: SeqLayout, latent, text_rows, mods, mod_final, rope_cos, rope_sin, key_mask,
                      dt: float, guidance: float, ws, skip_neg=None, rope_bstride: int = 0, stream=None):
+        """skip_neg: optional host sequence of n_blocks flags (the negative element bypasses a flagged block)."""
+        sk = None
+        if skip_neg is not None:
+            flags = [1 if bool(v) else 0 for v in (skip_neg.tolist() if hasattr(skip_neg, "tolist") else skip_neg)]
+            sk = (ctypes.c_uint8 * len(flags))(*flags)
         _check(lib().mi_denoise_step(self.handle, ctypes.byref(layout), _ptr(latent, _BF), _ptr(text_rows, _BF),
                                      _ptr(mods, _BF), _ptr(mod_final, _BF), _ptr(rope_cos, torch.float32),
                                      _ptr(rope_sin, torch.float32), rope_bstride, _ptr(key_mask, torch.uint8),
-                                     dt, guidance, _ptr(skip_neg, torch.uint8), _ptr(ws),
+                                     dt, guidance, ctypes.cast(sk, _P) if sk is not None else None, _ptr(ws),
                                      ws.numel() * ws.element_size(), _stream(stream)))
 
 

@@ -251,8 +251,8 @@ static mi_status block_forward_impl(mi_block* blk, int batch, int S, const void*
   const int H = d.hidden, I = d.mlp_inter, nh = d.n_heads;
   const int R = batch * S;
   const WsLayout w = plan_ws(d, batch, S);
-  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 1023u) != 0)
-    return fail(MI_ERR_WORKSPACE, "workspace must be non-null and 1024-byte aligned");
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(MI_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
   if (ws_bytes < w.total) return fail(MI_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, w.total);
   uint8_t* base = static_cast<uint8_t*>(ws);
   bf16* h = mb(base + w.off[MI_T_H]);
@@ -555,8 +555,8 @@ mi_status mi_denoise_step(mi_model* model, const mi_seq_layout* L, void* latent,
   const int N = L->grid_h * L->grid_w;
   if (N <= 0) return fail(MI_ERR_INVALID_ARG, "a denoising step needs image tokens");
   const StepLayout sl = plan_step(model, L->batch, S, N);
-  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 1023u) != 0)
-    return fail(MI_ERR_WORKSPACE, "workspace must be non-null and 1024-byte aligned");
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(MI_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
   if (ws_bytes < sl.total) return fail(MI_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, sl.total);
   DeviceInfo* dev = nullptr;
   st = require_sm103(&dev);

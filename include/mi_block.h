@@ -131,7 +131,8 @@ mi_status mi_block_tensor_offset(const mi_block* blk, int batch, int seq, int wh
  *            rope_bstride = 0 shares one table); pair p of row s rotates by the angle at [s, p]
  *   key_mask uint8 [B, S]: 0 excludes the key row from attention (padded prompt rows), or NULL.
  *            A query row whose keys are all masked gets a zero attention output.
- *   ws       device workspace of at least mi_block_workspace_size bytes, 1024-byte aligned
+ *   ws       device workspace of at least mi_block_workspace_size bytes, 256-byte aligned
+ *            (cudaMalloc and the PyTorch allocator both give at least that)
  */
 mi_status mi_block_forward(mi_block* blk, const mi_seq_layout* L, const void* x, void* y, const void* mod,
                            const float* rope_cos, const float* rope_sin, int rope_bstride,
@@ -164,7 +165,8 @@ mi_status mi_model_workspace_size(const mi_model* model, const mi_seq_layout* L,
  *   text_rows bf16 [B, T, H]
  *   mods      bf16 [n_blocks, B, 6, H] (per block, as in mi_block_forward)
  *   mod_final bf16 [B, 2, H]: shift_f, scale_f
- *   skip_neg  uint8 [n_blocks] or NULL: a nonzero entry makes the negative element bypass that block
+ *   skip_neg  HOST uint8 [n_blocks] or NULL (read on the host while enqueueing): a nonzero entry
+ *             makes the negative element (index 1) bypass that block
  */
 mi_status mi_denoise_step(mi_model* model, const mi_seq_layout* L, void* latent, const void* text_rows,
                           const void* mods, const void* mod_final, const float* rope_cos, const float* rope_sin,

@@ -31,7 +31,7 @@ class GpuStep:
         self.ws = torch.empty(self.model.workspace_size(self.layout), dtype=torch.uint8, device="cuda")
 
     def step(self, latent, dt, guidance, skip_neg=None):
-        sk = None if skip_neg is None else to_dev(np.asarray(skip_neg, dtype=np.uint8))
+        sk = None if skip_neg is None else np.asarray(skip_neg, dtype=np.uint8)
         self.model.denoise_step(self.layout, latent, self.text, self.mods, self.mod_final, self.cos, self.sin,
                                 self.mask, dt, guidance, self.ws, skip_neg=sk)
 
