@@ -232,7 +232,8 @@ class Model:
         if skip_neg is not None:
             flags = [1 if bool(v) else 0 for v in (skip_neg.tolist() if hasattr(skip_neg, "tolist") else skip_neg)]
             sk = (ctypes.c_uint8 * len(flags))(*flags)
-        _check(lib().mi_denoise_step(self.handle, ctypes.byref(layout), _ptr(latent, _BF), _ptr(text_rows, _BF),
+        _check(lib().mi_denoise_step(self.handle, ctypes.byref(layout), _ptr(latent, torch.float32),
+                                     _ptr(text_rows, _BF),
                                      _ptr(mods, _BF), _ptr(mod_final, _BF), _ptr(rope_cos, torch.float32),
                                      _ptr(rope_sin, torch.float32), rope_bstride, _ptr(key_mask, torch.uint8),
                                      dt, guidance, ctypes.cast(sk, _P) if sk is not None else None, _ptr(ws),

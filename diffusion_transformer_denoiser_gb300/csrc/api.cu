@@ -463,13 +463,15 @@ struct mi_model {
 };
 
 struct StepLayout {
-  size_t u, x, hf, vel, blk, total;
+  size_t lat16, u, x, hf, vel, blk, total;
 };
 
 static StepLayout plan_step(const mi_model* m, int batch, int S, int n_img) {
   StepLayout l;
   const size_t H = m->hidden, C = m->latent_ch;
   size_t cur = 0;
+  l.lat16 = cur;
+  cur = align_up(cur + (size_t)n_img * C * 2, 1024);
   l.u = cur;
   cur = align_up(cur + (size_t)n_img * H * 2, 1024);
   l.x = cur;
@@ -477,7 +479,7 @@ static StepLayout plan_step(const mi_model* m, int batch, int S, int n_img) {
   l.hf = cur;
   cur = align_up(cur + (size_t)batch * n_img * H * 2, 1024);
   l.vel = cur;
-  cur = align_up(cur + (size_t)batch * n_img * C * 2, 1024);
+  cur = align_up(cur + (size_t)batch * n_img * C * 4, 1024);
   l.blk = cur;
   cur += plan_ws(m->blocks[0]->d, batch, S).total;
   l.total = align_up(cur, 1024);
@@ -567,15 +569,18 @@ mi_status mi_denoise_step(mi_model* model, const mi_seq_layout* L, void* latent,
   bf16* u = mb(base + sl.u);
   bf16* x = mb(base + sl.x);
   bf16* hf = mb(base + sl.hf);
-  bf16* vel = mb(base + sl.vel);
+  bf16* lat16 = mb(base + sl.lat16);
+  float* vel = reinterpret_cast<float*>(base + sl.vel);
   void* bws = base + sl.blk;
   const size_t bws_bytes = ws_bytes - sl.blk;
   cudaError_t e;
 
-  // latent embedding u = latent W_in^T, then x_b = [text_b ; u]
+  // latent embedding u = bf16(latent) W_in^T, then x_b = [text_b ; u]
+  e = mi::f32_to_bf16_launch(static_cast<const float*>(latent), lat16, (size_t)N * C, s);
+  if (e != cudaSuccess) return cuda_fail(e, "latent cast");
   {
     CUtensorMap ta;
-    if (!map_a(&ta, latent, N, C)) return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed (latent)");
+    if (!map_a(&ta, lat16, N, C)) return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed (latent)");
     mi::GemmArgs g = gemm_args(N, H, C, u, dev->err);
     st = run_gemm(dev, mi::EPI_STORE, ta, model->tm_win, g, s);
     if (st != MI_OK) return st;
@@ -601,11 +606,11 @@ mi_status mi_denoise_step(mi_model* model, const mi_seq_layout* L, void* latent,
   {
     CUtensorMap ta;
     if (!map_a(&ta, hf, B * N, H)) return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed (final rows)");
-    mi::GemmArgs g = gemm_args(B * N, C, H, vel, dev->err);
-    st = run_gemm(dev, mi::EPI_STORE, ta, model->tm_wout, g, s);
+    mi::GemmArgs g = gemm_args(B * N, C, H, vel, dev->err);  // fp32 velocities (ldc = C floats)
+    st = run_gemm(dev, mi::EPI_STORE_F32, ta, model->tm_wout, g, s);
     if (st != MI_OK) return st;
   }
-  e = mi::cfg_euler_launch(vel, mb(latent), N, C, dt, guidance, B, s);
+  e = mi::cfg_euler_launch(vel, static_cast<float*>(latent), N, C, dt, guidance, B, s);
   if (e != cudaSuccess) return cuda_fail(e, "cfg_euler");
   return MI_OK;
 }

@@ -2,18 +2,25 @@
 //
 // The pages run the block's attention through a templated head-128 attention kernel with fp32
 // softmax (MOSS-Image transformer on CUDA, "What it adds" and "Shared code").  This kernel is
-// written for the 5th-generation tensor cores.  One CTA owns 128 query rows of one (batch, head):
-//   * warp 0   : TMA producer: the Q tile once, then K and V tiles of 128 keys into a 2-stage ring.
-//                K comes from the packed [B, heads, S, 128] rows written by the q/k norm + rotary
-//                kernel; V is read in place from the QKV projection output through a strided map.
-//   * warp 1   : one thread issues S = Q K^T (M=128, N=128, K=128) into one of two TMEM score
-//                buffers, and O += P V (B operand MN-major) into the TMEM output accumulator.
-//   * warps 2-5: one thread per query row: scores from TMEM, key tail / key mask as -inf, running
-//                max and sum in fp32 (base-2 with log2(e)/sqrt(128) folded in), P as bf16 into a
-//                128-byte-swizzled shared tile, O rescaled in TMEM when the max moves, and the
-//                final O / l written as bf16.
-// S for tile j+1 is computed while the softmax works on tile j.  Tile order is fixed, so results
-// repeat bit for bit.
+// written for the 5th-generation tensor cores.  One CTA owns two 128-row query tiles of one
+// (batch, head) and streams the keys once for both:
+//   * warp 0   : TMA producer: both Q tiles once, then K and V tiles of 128 keys into a 2-stage
+//                ring (K and V with their own barriers so a K slot frees as soon as both score
+//                products have read it).  K comes from the packed [B, heads, S, 128] rows; V is
+//                read in place from the QKV projection output through a strided 4-D map.
+//   * warp 1   : one thread issues, per key tile j, in this order
+//                  O0 += P0 V_j,  S0 = Q0 K_{j+1}^T,  O1 += P1 V_j,  S1 = Q1 K_{j+1}^T
+//                so the tensor core works on one query tile while the softmax works on the other.
+//   * warps 2-5 (query tile 0) and 6-9 (query tile 1): one thread per query row.  Scores come
+//                from TMEM; the key tail and masked keys become -inf; the running max lives in
+//                base 2 with log2(e)/sqrt(128) folded into one FMA; P is rounded to bf16 and
+//                written back into TMEM over the scores, where it is the A operand of P V.  O is
+//                rescaled in TMEM only when a row's max grows by more than 2^8 (the stale max
+//                keeps every exponent <= 2^8, so P stays exact enough in bf16 and the sum in fp32).
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); P_i = first 64
+// columns of S_i.  tcgen05.mma operations of one thread execute in issue order, so S_i(j+1) may be
+// issued right after the P_i(j) V_j product that still reads P_i(j) from the same columns.  Tile
+// order and reduction order are fixed: results repeat bit for bit.
 #include "mi_internal.h"
 #include "ptx.cuh"
 
@@ -23,20 +30,20 @@ namespace {
 
 constexpr int BQ = 128;
 constexpr int BKV = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128 x 128 bf16 tile = two 16 KB swizzled halves
 constexpr int HALF_BYTES = TILE_BYTES / 2;
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE_BYTES;        // 2 stages
-constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;    // 2 stages
-constexpr int OFF_P = OFF_V + 2 * TILE_BYTES;
-constexpr int OFF_BAR = OFF_P + TILE_BYTES;
+constexpr int OFF_Q = 0;                        // 2 query tiles
+constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;   // 2 stages
+constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;   // 2 stages
+constexpr int OFF_BAR = OFF_V + 2 * TILE_BYTES;
 constexpr int SMEM_TOTAL = OFF_BAR + 256 + 1024;
 
-constexpr uint32_t TM_S0 = 0;
-constexpr uint32_t TM_O = 256;
+constexpr uint32_t TM_S = 0;    // S_i at TM_S + 128 i (P_i in its first 64 columns)
+constexpr uint32_t TM_O = 256;  // O_i at TM_O + 128 i
 constexpr uint32_t TM_COLS = 512;
+constexpr float kRescaleLog2 = 8.0f;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
@@ -48,27 +55,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem + OFF_Q;
   uint8_t* sK = smem + OFF_K;
   uint8_t* sV = smem + OFF_V;
-  uint8_t* sP = smem + OFF_P;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;    // [2]
   uint64_t* v_full = bars + 3;    // [2]
-  uint64_t* kv_empty = bars + 5;  // [2]
-  uint64_t* s_full = bars + 7;    // [2]
-  uint64_t* s_empty = bars + 9;   // [2]
-  uint64_t* p_full = bars + 11;
-  uint64_t* o_ready = bars + 12;
-  uint64_t* drain = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* k_empty = bars + 5;   // [2]
+  uint64_t* v_empty = bars + 7;   // [2]
+  uint64_t* s_full = bars + 9;    // [2] per query tile
+  uint64_t* p_full = bars + 11;   // [2] per query tile
+  uint64_t* o_done = bars + 13;   // [2] per query tile
+  uint64_t* drain = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt = blockIdx.x;
   const int h = blockIdx.y;
   const int b = blockIdx.z;
   const int S = p.seq;
-  const int q0 = qt * BQ;
+  const int q0 = blockIdx.x * (2 * BQ);
   const int n_kv = (S + BKV - 1) / BKV;
   const int bh = b * p.n_heads + h;
 
@@ -77,12 +82,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&v_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&o_done[i], 1);
     }
-    mbar_init(p_full, 4);
-    mbar_init(o_ready, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -102,29 +107,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(q_full, TILE_BYTES);
+      mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
       tma_load_3d(sQ, &tmQ, q_full, 0, q0, bh);
       tma_load_3d(sQ + HALF_BYTES, &tmQ, q_full, 64, q0, bh);
-      int issued = 0;
+      tma_load_3d(sQ + TILE_BYTES, &tmQ, q_full, 0, q0 + BQ, bh);
+      tma_load_3d(sQ + TILE_BYTES + HALF_BYTES, &tmQ, q_full, 64, q0 + BQ, bh);
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j & 1;
-        if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 1)) break;
+        const uint32_t ph = (uint32_t)((j >> 1) & 1);
+        if (!mbar_wait(&k_empty[st], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ATTN + 1)) break;
         uint8_t* k_dst = sK + st * TILE_BYTES;
-        uint8_t* v_dst = sV + st * TILE_BYTES;
         mbar_arrive_expect_tx(&k_full[st], TILE_BYTES);
         tma_load_3d(k_dst, &tmK, &k_full[st], 0, j * BKV, bh);
         tma_load_3d(k_dst + HALF_BYTES, &tmK, &k_full[st], 64, j * BKV, bh);
+        k_issued = j + 1;
+        if (!mbar_wait(&v_empty[st], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ATTN + 1)) break;
+        uint8_t* v_dst = sV + st * TILE_BYTES;
         mbar_arrive_expect_tx(&v_full[st], TILE_BYTES);
         tma_load_4d(v_dst, &tmV, &v_full[st], 0, h, j * BKV, b);
         tma_load_4d(v_dst + HALF_BYTES, &tmV, &v_full[st], 64, h, j * BKV, b);
-        issued = j + 1;
+        v_issued = j + 1;
       }
-      // drain the copies still in flight: the last use of stage st is tile (issued-1 or issued-2)
+      // drain the copies still in flight (the last use of each stage)
       mbar_wait_drain(q_full, 0, p.err, DEV_TIMEOUT_ATTN + 2);
-      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) {
+      for (int j = k_issued - 2 < 0 ? 0 : k_issued - 2; j < k_issued; ++j)
         mbar_wait_drain(&k_full[j & 1], (j >> 1) & 1, p.err, DEV_TIMEOUT_ATTN + 2);
+      for (int j = v_issued - 2 < 0 ? 0 : v_issued - 2; j < v_issued; ++j)
         mbar_wait_drain(&v_full[j & 1], (j >> 1) & 1, p.err, DEV_TIMEOUT_ATTN + 2);
-      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -132,83 +142,102 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
       const uint32_t q_addr = smem_u32(sQ);
-      const uint32_t p_addr = smem_u32(sP);
-      auto issue_qk = [&](int j) {
-        const uint32_t k_addr = smem_u32(sK + (j & 1) * TILE_BYTES);
-        const uint32_t d = tmem_base + TM_S0 + (uint32_t)(j & 1) * 128u;
+      auto issue_s = [&](int i, int j) {  // S_i = Q_i K_j^T
+        const uint32_t qa = q_addr + (uint32_t)i * TILE_BYTES;
+        const uint32_t ka = smem_u32(sK + (j & 1) * TILE_BYTES);
+        const uint32_t d = tmem_base + TM_S + (uint32_t)i * 128u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u;
-          tc_mma_ss(d, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc_qk,
-                    kk > 0 ? 1u : 0u);
+          tc_mma_ss(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int i, int j) {  // O_i += P_i V_j, P_i from TMEM
+        const uint32_t va = smem_u32(sV + (j & 1) * TILE_BYTES);
+        const uint32_t pa = tmem_base + TM_S + (uint32_t)i * 128u;
+        const uint32_t d = tmem_base + TM_O + (uint32_t)i * 128u;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // 16 keys per step: 8 packed P columns; V is MN-major (two 8-key groups 1024 B apart,
+          // d halves 16 KB apart)
+          tc_mma_ts(d, pa + (uint32_t)kk * 8u, sdesc_sw128(va + (uint32_t)kk * 2048u, HALF_BYTES, 1024), idesc_pv,
+                    (j > 0 || kk > 0) ? 1u : 0u);
         }
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, p.err, DEV_TIMEOUT_ATTN + 3) &&
                 mbar_wait(&k_full[0], 0, abort_flag, p.err, DEV_TIMEOUT_ATTN + 3);
       if (ok) {
         tc_fence_after();
-        issue_qk(0);
+        issue_s(0, 0);
         tc_commit(&s_full[0]);
+        issue_s(1, 0);
+        tc_commit(&s_full[1]);
+        tc_commit(&k_empty[0]);
       }
       for (int j = 0; j < n_kv && ok; ++j) {
-        if (j + 1 < n_kv) {
-          const int nb = (j + 1) & 1;
-          const uint32_t use = (uint32_t)((j + 1) >> 1);
-          if (!mbar_wait(&s_empty[nb], (use & 1u) ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4) ||
-              !mbar_wait(&k_full[nb], use & 1u, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_qk(j + 1);
-          tc_commit(&s_full[nb]);
-        }
         const int st = j & 1;
-        if (!mbar_wait(p_full, j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 5) ||
-            !mbar_wait(&v_full[st], (j >> 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 5)) {
+        const uint32_t ph = (uint32_t)((j >> 1) & 1);
+        const bool more = j + 1 < n_kv;
+        const int nst = (j + 1) & 1;
+        const uint32_t nph = (uint32_t)(((j + 1) >> 1) & 1);
+        // query tile 0
+        if (!mbar_wait(&p_full[0], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4) ||
+            !mbar_wait(&v_full[st], ph, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(sV + st * TILE_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t a_off = (uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u;
-          // V is MN-major: 16 keys = two 8-row groups (SBO 1024); d halves 16 KB apart (LBO)
-          tc_mma_ss(tmem_base + TM_O, sdesc_sw128(p_addr + a_off, 16, 1024),
-                    sdesc_sw128(v_addr + (uint32_t)kk * 2048u, HALF_BYTES, 1024), idesc_pv,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+        issue_pv(0, j);
+        tc_commit(&o_done[0]);
+        if (more) {
+          if (!mbar_wait(&k_full[nst], nph, abort_flag, p.err, DEV_TIMEOUT_ATTN + 5)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(0, j + 1);
+          tc_commit(&s_full[0]);
         }
-        tc_commit(&kv_empty[st]);
-        tc_commit(o_ready);
+        // query tile 1
+        if (!mbar_wait(&p_full[1], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 6)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(1, j);
+        tc_commit(&o_done[1]);
+        tc_commit(&v_empty[st]);
+        if (more) {
+          issue_s(1, j + 1);
+          tc_commit(&s_full[1]);
+          tc_commit(&k_empty[nst]);
+        }
       }
       tc_commit(drain);
-      mbar_wait_drain(drain, 0, p.err, DEV_TIMEOUT_ATTN + 6);
+      mbar_wait_drain(drain, 0, p.err, DEV_TIMEOUT_ATTN + 7);
     }
   } else {
     // ------------------------------------------------------------------ softmax / epilogue
-    const int qw = warp & 3;
-    const int r = qw * 32 + lane;  // query row inside the tile == TMEM lane
+    const int wg = (warp - 2) >> 2;  // query tile of this warpgroup
+    const int qw = warp & 3;         // TMEM lane quarter of this warp
+    const int r = qw * 32 + lane;    // query row inside the tile == TMEM lane
     const uint32_t t_lane = tmem_base + ((uint32_t)(qw * 32) << 16);
+    const uint32_t t_s = t_lane + TM_S + (uint32_t)wg * 128u;
+    const uint32_t t_o = t_lane + TM_O + (uint32_t)wg * 128u;
     const float sl2 = p.scale_log2;
-    float m_run = neg_inf();
+    float m_run = neg_inf();  // reference max (base-2 units) the exponents are taken against
     float l_run = 0.0f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait_warp(&s_full[sb], (j >> 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 7)) {
+      if (!mbar_wait_warp(&s_full[wg], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 8)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sr[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(t_lane + TM_S0 + sb * 128 + c * 32, sr + c * 32);
+      for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr + c * 32);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[sb]);
-
       float* s = reinterpret_cast<float*>(sr);
       const int kbase = j * BKV;
       if (p.key_mask != nullptr || kbase + BKV > S) {
@@ -227,66 +256,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mx = s[0];
 #pragma unroll
       for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-      const float m_new = fmaxf(m_run, mx * sl2);
-      const float m_use = (m_new == neg_inf()) ? 0.0f : m_new;
-      const float alpha = ex2_approx(m_run - m_use);
+      const float m_cand = mx * sl2;
+      float alpha = 1.0f;
+      const bool grow = m_cand > m_run + kRescaleLog2;  // also true for the first finite max
+      if (grow) {
+        alpha = ex2_approx(m_run - m_cand);
+        m_run = m_cand;
+      }
+      const float m_use = (m_run == neg_inf()) ? 0.0f : m_run;
       float sum = 0.0f;
+      uint32_t pk[64];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float e = ex2_approx(fmaf(s[c], sl2, -m_use));
-        s[c] = e;
-        sum += e;
+      for (int c = 0; c < 64; ++c) {
+        const float e0 = ex2_approx(fmaf(s[2 * c], sl2, -m_use));
+        const float e1 = ex2_approx(fmaf(s[2 * c + 1], sl2, -m_use));
+        sum += e0;
+        sum += e1;
+        pk[c] = pack_bf16x2(e0, e1);
       }
       l_run = l_run * alpha + sum;
-      m_run = m_new;
 
       if (j > 0) {
-        // the previous P V product must be done before O is rescaled and P is overwritten
-        if (!mbar_wait_warp(o_ready, (j - 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 8)) {
+        // the previous P V product is complete (S_i(j) was issued after it); keep the phases of
+        // o_done in step with the loop
+        if (!mbar_wait_warp(&o_done[wg], (j - 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 9)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+        if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
-            tmem_ld32(t_lane + TM_O + c * 32, o);
+            tmem_ld32(t_o + c * 32, o);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(t_lane + TM_O + c * 32, o);
+            tmem_st32(t_o + c * 32, o);
           }
-          tmem_st_wait();
         }
       }
-      // P row -> swizzled K-major tile (two 64-key halves, 128 B per row, 16-B chunks XOR row%8)
-#pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        const uint32_t off = (uint32_t)(c8 >> 3) * HALF_BYTES + (uint32_t)r * 128u +
-                             ((uint32_t)((c8 & 7) ^ (r & 7)) << 4);
-        uint4 v;
-        v.x = pack_bf16x2(s[c8 * 8 + 0], s[c8 * 8 + 1]);
-        v.y = pack_bf16x2(s[c8 * 8 + 2], s[c8 * 8 + 3]);
-        v.z = pack_bf16x2(s[c8 * 8 + 4], s[c8 * 8 + 5]);
-        v.w = pack_bf16x2(s[c8 * 8 + 6], s[c8 * 8 + 7]);
-        *reinterpret_cast<uint4*>(sP + off) = v;
-      }
-      fence_proxy_async_smem();
+      // P (bf16) over the first 64 columns of S_i
+      tmem_st32(t_s, pk);
+      tmem_st32(t_s + 32, pk + 32);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[wg]);
     }
-    if (ok && mbar_wait_warp(o_ready, (n_kv - 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 9)) {
+    if (ok && mbar_wait_warp(&o_done[wg], (n_kv - 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 10)) {
       tc_fence_after();
       const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
-      const int row = q0 + r;
+      const int row = q0 + wg * BQ + r;
       const int H = p.n_heads * kHeadDim;
       __nv_bfloat16* dst_row = p.out + ((size_t)b * S + row) * H + (size_t)h * kHeadDim;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
-        tmem_ld32(t_lane + TM_O + c * 32, o);
+        tmem_ld32(t_o + c * 32, o);
         tmem_ld_wait();
         if (row < S) {
           uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
@@ -326,7 +353,7 @@ cudaError_t attention_launch(const CUtensorMap& tq, const CUtensorMap& tk, const
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  dim3 grid((a.seq + BQ - 1) / BQ, a.n_heads, a.batch);
+  dim3 grid((a.seq + 2 * BQ - 1) / (2 * BQ), a.n_heads, a.batch);
   attn_fwd_kernel<<<grid, kThreads, SMEM_TOTAL, s>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }

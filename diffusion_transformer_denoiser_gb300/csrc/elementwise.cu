@@ -198,16 +198,22 @@ __global__ void __launch_bounds__(256) copy_vec_kernel(const uint4* __restrict__
     dst[i] = src[i];
 }
 
-// v = v_neg + g (v_pos - v_neg) in fp32, latent <- bf16(latent + dt v).  vel is [2, N, C].
-__global__ void __launch_bounds__(256) cfg_euler_kernel(const __nv_bfloat16* __restrict__ vel,
-                                                        __nv_bfloat16* __restrict__ latent, long long n, float dt,
-                                                        float guidance, int batch) {
+// v = v_neg + g (v_pos - v_neg), latent <- latent + dt v, all fp32.  vel is [batch, N, C].
+__global__ void __launch_bounds__(256) cfg_euler_kernel(const float* __restrict__ vel, float* __restrict__ latent,
+                                                        long long n, float dt, float guidance, int batch) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
-    const float vp = __bfloat162float(vel[i]);
-    const float v = batch > 1 ? fmaf(guidance, vp - __bfloat162float(vel[n + i]), __bfloat162float(vel[n + i])) : vp;
-    latent[i] = __float2bfloat16_rn(fmaf(dt, v, __bfloat162float(latent[i])));
+    const float vp = vel[i];
+    const float v = batch > 1 ? fmaf(guidance, vp - vel[n + i], vel[n + i]) : vp;
+    latent[i] = fmaf(dt, v, latent[i]);
   }
+}
+
+__global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+                                                          long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    dst[i] = __float2bfloat16_rn(src[i]);
 }
 
 int grid_for(long long work_items, int threads) {
@@ -287,11 +293,17 @@ cudaError_t copy_rows_launch(const __nv_bfloat16* src, __nv_bfloat16* dst, size_
   return cudaGetLastError();
 }
 
-cudaError_t cfg_euler_launch(const __nv_bfloat16* vel, __nv_bfloat16* latent, int n_img, int channels, float dt,
-                             float guidance, int batch, cudaStream_t s) {
+cudaError_t cfg_euler_launch(const float* vel, float* latent, int n_img, int channels, float dt, float guidance,
+                             int batch, cudaStream_t s) {
   const long long n = (long long)n_img * channels;
   if (n <= 0) return cudaSuccess;
   cfg_euler_kernel<<<grid_for(n, 256), 256, 0, s>>>(vel, latent, n, dt, guidance, batch);
+  return cudaGetLastError();
+}
+
+cudaError_t f32_to_bf16_launch(const float* src, __nv_bfloat16* dst, size_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  f32_to_bf16_kernel<<<grid_for((long long)n, 256), 256, 0, s>>>(src, dst, (long long)n);
   return cudaGetLastError();
 }
 

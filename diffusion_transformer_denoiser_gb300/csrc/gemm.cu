@@ -213,7 +213,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t_row + c * 32, r);
           tmem_ld_wait();
           const int col0 = nb * BN + c * 32;
-          if (row_ok && col0 < p.N) {
+          if (EPI == EPI_STORE_F32) {
+            if (row_ok && col0 < p.N) {
+              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.C) + (size_t)row * p.ldc + col0);
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                if (col0 + v * 4 < p.N)
+                  dst[v] = make_float4(__uint_as_float(r[v * 4 + 0]), __uint_as_float(r[v * 4 + 1]),
+                                       __uint_as_float(r[v * 4 + 2]), __uint_as_float(r[v * 4 + 3]));
+              }
+            }
+          } else if (row_ok && col0 < p.N) {
             uint4* dst = reinterpret_cast<uint4*>(p.C + (size_t)row * p.ldc + col0);
             if (EPI == EPI_GATED_RESIDUAL) {
               const uint4* xr = reinterpret_cast<const uint4*>(p.resid + (size_t)row * p.ldr + col0);
@@ -304,6 +314,8 @@ cudaError_t gemm_launch(int epi, const CUtensorMap& ta, const CUtensorMap& tb, c
       return launch_gemm<256, EPI_GATED_RESIDUAL>(ta, tb, a, num_sms, s);
     case EPI_SILU_GATE:
       return launch_gemm<256, EPI_SILU_GATE>(ta, tb, a, num_sms, s);
+    case EPI_STORE_F32:
+      return launch_gemm<256, EPI_STORE_F32>(ta, tb, a, num_sms, s);
     default:
       return cudaErrorInvalidValue;
   }

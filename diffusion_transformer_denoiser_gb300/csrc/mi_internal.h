@@ -16,6 +16,7 @@ enum GemmEpilogue : int {
   EPI_STORE = 0,           // C = A W^T
   EPI_GATED_RESIDUAL = 1,  // C = resid + gate[b] * bf16(A W^T)
   EPI_SILU_GATE = 2,       // C[:, j] = silu(bf16(A Wg^T)[:, j]) * bf16(A Wu^T)[:, j], W = [Wg; Wu]
+  EPI_STORE_F32 = 3,       // C (fp32) = A W^T, the fp32 sums unrounded (C is a float*, ldc in floats)
 };
 
 struct GemmArgs {
@@ -61,8 +62,9 @@ cudaError_t mod_rmsnorm_rows_launch(const __nv_bfloat16* x, const __nv_bfloat16*
                                     int mod_bstride, __nv_bfloat16* out, int rows, int out_seq, int in_seq, int in_off,
                                     int hidden, float eps, cudaStream_t s);
 cudaError_t copy_rows_launch(const __nv_bfloat16* src, __nv_bfloat16* dst, size_t n_elems, cudaStream_t s);
-cudaError_t cfg_euler_launch(const __nv_bfloat16* vel, __nv_bfloat16* latent, int n_img, int channels, float dt,
-                             float guidance, int batch, cudaStream_t s);
+cudaError_t cfg_euler_launch(const float* vel, float* latent, int n_img, int channels, float dt, float guidance,
+                             int batch, cudaStream_t s);
+cudaError_t f32_to_bf16_launch(const float* src, __nv_bfloat16* dst, size_t n, cudaStream_t s);
 
 // Tensor maps (tmap.cpp).
 bool encode_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,

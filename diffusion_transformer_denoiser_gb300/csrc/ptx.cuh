@@ -181,6 +181,18 @@ __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t adesc, uint6
       : "memory");
 }
 
+// D(tmem) (+)= A(tmem) * B(smem): A is M x K with row m in TMEM lane m and K packed two bf16 per
+// 32-bit column (element k in column k/2, low half for even k).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor of a 128-byte-swizzled operand tile.
 //   start: shared address of the (1024-byte aligned) atom the operand starts in, plus the byte
 //          offset of the K slice inside the 128-byte row (multiples of 32 bytes for bf16 K=16);

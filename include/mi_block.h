@@ -161,7 +161,8 @@ mi_status mi_model_workspace_size(const mi_model* model, const mi_seq_layout* L,
  *   vel_b = (RMSNorm(image rows of x_b) (1 + scale_f) + shift_f) W_out^T;
  *   v = vel_1 + guidance (vel_0 - vel_1) when batch == 2 (element 0 the prompt, 1 the negative),
  *   v = vel_0 when batch == 1;  latent <- latent + dt v.
- *   latent    bf16 [N, C] (N = grid_h * grid_w), updated in place
+ *   latent    fp32 [N, C] (N = grid_h * grid_w), the Euler state, updated in place in fp32; the
+ *             embedding reads it rounded to bf16.  The velocities stay fp32 (unrounded GEMM sums).
  *   text_rows bf16 [B, T, H]
  *   mods      bf16 [n_blocks, B, 6, H] (per block, as in mi_block_forward)
  *   mod_final bf16 [B, 2, H]: shift_f, scale_f

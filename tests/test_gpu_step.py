@@ -48,7 +48,7 @@ def test_step_velocity_parity():
     mi = require_gpu()
     si = mi_synth.step_inputs(mi_synth.GEOMETRIES["step_tiny_cfg"], 0)
     gs = GpuStep(mi, si)
-    lat = to_dev_bf16(si.latent)
+    lat = to_dev(mi_synth.bits_to_f32(si.latent))
     gs.step(lat, 1.0, 3.0)
     torch.cuda.synchronize()
     assert mi.device_error() == 0
@@ -60,7 +60,7 @@ def test_step_parity_default_schedule():
     mi = require_gpu()
     si = mi_synth.step_inputs(mi_synth.GEOMETRIES["step_tiny_cfg"], 1)
     gs = GpuStep(mi, si)
-    lat = to_dev_bf16(si.latent)
+    lat = to_dev(mi_synth.bits_to_f32(si.latent))
     gs.step(lat, -0.02, 3.0)
     new, _, _ = _oracle_step(si, -0.02, 3.0)
     assert_parity(to_f64(lat), new, "latent")
@@ -72,7 +72,7 @@ def test_step_skip_negative_block():
     skip = np.zeros(si.geom.n_blocks, dtype=bool)
     skip[22] = True
     gs = GpuStep(mi, si)
-    lat = to_dev_bf16(si.latent)
+    lat = to_dev(mi_synth.bits_to_f32(si.latent))
     gs.step(lat, 1.0, 3.0, skip_neg=skip)
     new, _, _ = _oracle_step(si, 1.0, 3.0, skip_neg=skip)
     assert_parity(to_f64(lat) - O.widen(si.latent), new - O.widen(si.latent), "velocity with block 22 skipped")
@@ -90,33 +90,52 @@ def test_step_batch_one_is_the_prompt_velocity():
     gs.mod_final = to_dev_bf16(si.mod_final[:1])
     gs.mask = to_dev(si.key_mask[:1])
     gs.text = to_dev_bf16(si.text_rows[:1])
-    lat = to_dev_bf16(si.latent)
+    lat = to_dev(mi_synth.bits_to_f32(si.latent))
     gs.step(lat, 1.0, 3.0)
     _, vp, _ = _oracle_step(si, 1.0, 3.0)
     assert_parity(to_f64(lat) - O.widen(si.latent), vp, "prompt velocity")
     assert g1.batch == 1
 
 
+@pytest.mark.parametrize("guidance", [1.0, 0.0], ids=["prompt_branch", "negative_branch"])
+def test_step_branch_velocities(guidance):
+    # guidance 1 gives v = v_pos and guidance 0 gives v = v_neg: each branch alone at the bar
+    mi = require_gpu()
+    si = mi_synth.step_inputs(mi_synth.GEOMETRIES["step_tiny_cfg"], 6)
+    gs = GpuStep(mi, si)
+    lat = to_dev(mi_synth.bits_to_f32(si.latent))
+    gs.step(lat, 1.0, guidance)
+    _, vp, vn = _oracle_step(si, 1.0, guidance)
+    assert_parity(to_f64(lat) - O.widen(si.latent), vp if guidance == 1.0 else vn, "branch velocity")
+
+
 def test_euler_loop_50_steps():
+    # every step is checked against the oracle step taken from the same (GPU) latent; the whole
+    # chain is then compared with the oracle's own 50-step chain
     mi = require_gpu()
     g = mi_synth.GEOMETRIES["loop_tiny_cfg50"]
     si = mi_synth.step_inputs(g, 4)
     gs = GpuStep(mi, si)
     ts = mi_synth.euler_schedule(g.n_steps)
-    lat = to_dev_bf16(si.latent)
+    lat = to_dev(mi_synth.bits_to_f32(si.latent))
+    hist = [to_f64(lat)]
     for i in range(g.n_steps):
         gs.step(lat, float(ts[i + 1] - ts[i]), g.guidance)
+        hist.append(to_f64(lat))
+    torch.cuda.synchronize()
+    assert mi.device_error() == 0
     a = O.step_inputs_widened(si)
+    for i in range(g.n_steps):
+        a["latent"] = hist[i]
+        ref = O.denoise_step(**a, dt=ts[i + 1] - ts[i], guidance=g.guidance)[0]
+        assert_parity(hist[i + 1] - hist[i], ref - hist[i], f"step {i} displacement")
 
     def step_fn(x, dt):
         a["latent"] = x
         return O.denoise_step(**a, dt=dt, guidance=g.guidance)[0]
 
-    ref = O.euler_loop(O.widen(si.latent), ts, step_fn)
-    torch.cuda.synchronize()
-    assert mi.device_error() == 0
-    assert_parity(to_f64(lat), ref, "latent after 50 steps")
-    assert_parity(to_f64(lat) - O.widen(si.latent), ref - O.widen(si.latent), "total displacement")
+    chain = O.euler_loop(O.widen(si.latent), ts, step_fn)
+    assert_parity(hist[-1], chain, "latent after 50 steps")
 
 
 def test_step_repeats_bit_for_bit():
@@ -125,7 +144,7 @@ def test_step_repeats_bit_for_bit():
     gs = GpuStep(mi, si)
     outs = []
     for _ in range(2):
-        lat = to_dev_bf16(si.latent)
+        lat = to_dev(mi_synth.bits_to_f32(si.latent))
         gs.step(lat, -0.02, 3.0)
-        outs.append(bf16_to_bits(lat))
+        outs.append(lat.cpu().numpy().copy())
     assert np.array_equal(outs[0], outs[1])
