@@ -253,9 +253,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (!((words[c >> 5] >> (c & 31)) & 1u)) s[c] = neg_inf();
       }
-      float mx = s[0];
+      // row max and (below) row sum with 8 independent partials: short dependency chains
+      float mp[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      for (int k = 0; k < 8; ++k) mp[k] = s[k];
+#pragma unroll
+      for (int c = 8; c < 128; c += 8) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[c + k]);
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       const float m_cand = mx * sl2;
       float alpha = 1.0f;
       const bool grow = m_cand > m_run + kRescaleLog2;  // also true for the first finite max
@@ -264,16 +272,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = m_cand;
       }
       const float m_use = (m_run == neg_inf()) ? 0.0f : m_run;
-      float sum = 0.0f;
+      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float e0 = ex2_approx(fmaf(s[2 * c], sl2, -m_use));
         const float e1 = ex2_approx(fmaf(s[2 * c + 1], sl2, -m_use));
-        sum += e0;
-        sum += e1;
+        sp[(2 * c) & 7] += e0;
+        sp[(2 * c + 1) & 7] += e1;
         pk[c] = pack_bf16x2(e0, e1);
       }
+      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       l_run = l_run * alpha + sum;
 
       if (j > 0) {

@@ -45,6 +45,23 @@ def assert_parity(got, ref, name=""):
     return cos, err / mref if mref > 0 else 0.0
 
 
+def assert_parity_combination(got, parts, name=""):
+    """Parity of a linear combination sum_k c_k ref_k whose parts each carry the per-tensor bar.
+
+    If every part ref_k is reproduced within cosine COS_MIN (relative L2 error at most
+    sqrt(2 (1 - COS_MIN))) and max-abs error REL_MAX * max|ref_k|, the combination's error is at most
+    the same combination of the parts' bounds: sum_k |c_k| * bound_k (triangle inequality).  Guided
+    velocities v = v_neg + g (v_pos - v_neg) = (1 - g) v_neg + g v_pos take this bar."""
+    ref = sum(c * r for c, r in parts)
+    e = np.asarray(got, dtype=np.float64).ravel() - np.asarray(ref, dtype=np.float64).ravel()
+    rel_l2 = np.sqrt(2.0 * (1.0 - COS_MIN))
+    l2_bound = sum(abs(c) * rel_l2 * np.linalg.norm(r) for c, r in parts)
+    max_bound = sum(abs(c) * REL_MAX * np.abs(r).max() for c, r in parts)
+    assert np.isfinite(got).all(), f"{name}: non-finite GPU output"
+    assert np.linalg.norm(e) <= l2_bound, f"{name}: |err|_2 {np.linalg.norm(e):.4g} > {l2_bound:.4g}"
+    assert np.abs(e).max() <= max_bound, f"{name}: max|err| {np.abs(e).max():.4g} > {max_bound:.4g}"
+
+
 def require_gpu():
     if not torch.cuda.is_available():
         pytest.skip("no GPU")

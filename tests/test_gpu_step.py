@@ -5,7 +5,8 @@ import torch
 
 import mi_synth
 from oracle import mi_oracle as O
-from tests._gpu import assert_parity, bf16_to_bits, require_gpu, to_dev, to_dev_bf16, to_f64
+from tests._gpu import (COS_MIN, REL_MAX, assert_parity, assert_parity_combination, require_gpu, to_dev,
+                        to_dev_bf16, to_f64)
 
 pytestmark = pytest.mark.gpu
 BF = torch.bfloat16
@@ -52,8 +53,9 @@ def test_step_velocity_parity():
     gs.step(lat, 1.0, 3.0)
     torch.cuda.synchronize()
     assert mi.device_error() == 0
-    new, vp, vn = _oracle_step(si, 1.0, 3.0)
-    assert_parity(to_f64(lat) - O.widen(si.latent), new - O.widen(si.latent), "guided velocity")
+    _, vp, vn = _oracle_step(si, 1.0, 3.0)
+    # v = (1 - g) v_neg + g v_pos: each branch carries the per-tensor bar, the combination their sum
+    assert_parity_combination(to_f64(lat) - O.widen(si.latent), [(-2.0, vn), (3.0, vp)], "guided velocity")
 
 
 def test_step_parity_default_schedule():
@@ -74,8 +76,9 @@ def test_step_skip_negative_block():
     gs = GpuStep(mi, si)
     lat = to_dev(mi_synth.bits_to_f32(si.latent))
     gs.step(lat, 1.0, 3.0, skip_neg=skip)
-    new, _, _ = _oracle_step(si, 1.0, 3.0, skip_neg=skip)
-    assert_parity(to_f64(lat) - O.widen(si.latent), new - O.widen(si.latent), "velocity with block 22 skipped")
+    _, vp, vn = _oracle_step(si, 1.0, 3.0, skip_neg=skip)
+    assert_parity_combination(to_f64(lat) - O.widen(si.latent), [(-2.0, vn), (3.0, vp)],
+                              "velocity with block 22 skipped")
 
 
 def test_step_batch_one_is_the_prompt_velocity():
@@ -125,17 +128,29 @@ def test_euler_loop_50_steps():
     torch.cuda.synchronize()
     assert mi.device_error() == 0
     a = O.step_inputs_widened(si)
+    gd = g.guidance
     for i in range(g.n_steps):
         a["latent"] = hist[i]
-        ref = O.denoise_step(**a, dt=ts[i + 1] - ts[i], guidance=g.guidance)[0]
-        assert_parity(hist[i + 1] - hist[i], ref - hist[i], f"step {i} displacement")
+        dt = ts[i + 1] - ts[i]
+        _, vp, vn = O.denoise_step(**a, dt=dt, guidance=gd)
+        assert_parity_combination(hist[i + 1] - hist[i], [(dt * (1 - gd), vn), (dt * gd, vp)],
+                                  f"step {i} displacement")
 
-    def step_fn(x, dt):
+    # the oracle's own chain; first-order bound: the per-step velocity bounds summed over the steps
+    x = O.widen(si.latent)
+    l2_bound = max_bound = 0.0
+    rel_l2 = np.sqrt(2.0 * (1.0 - COS_MIN))
+    for i in range(g.n_steps):
         a["latent"] = x
-        return O.denoise_step(**a, dt=dt, guidance=g.guidance)[0]
-
-    chain = O.euler_loop(O.widen(si.latent), ts, step_fn)
-    assert_parity(hist[-1], chain, "latent after 50 steps")
+        dt = ts[i + 1] - ts[i]
+        x, vp, vn = O.denoise_step(**a, dt=dt, guidance=gd)
+        l2_bound += abs(dt) * rel_l2 * (abs(1 - gd) * np.linalg.norm(vn) + abs(gd) * np.linalg.norm(vp))
+        max_bound += abs(dt) * REL_MAX * (abs(1 - gd) * np.abs(vn).max() + abs(gd) * np.abs(vp).max())
+    e = hist[-1] - x
+    print(f"50-step chain: |err|_2 {np.linalg.norm(e):.4g} (bound {l2_bound:.4g}), "
+          f"max|err| {np.abs(e).max():.4g} (bound {max_bound:.4g})")
+    assert np.linalg.norm(e) <= l2_bound and np.abs(e).max() <= max_bound
+    assert_parity(hist[-1], x, "latent after 50 steps")
 
 
 def test_step_repeats_bit_for_bit():
@@ -147,4 +162,4 @@ def test_step_repeats_bit_for_bit():
         lat = to_dev(mi_synth.bits_to_f32(si.latent))
         gs.step(lat, -0.02, 3.0)
         outs.append(lat.cpu().numpy().copy())
-    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
