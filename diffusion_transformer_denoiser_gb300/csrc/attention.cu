@@ -37,7 +37,9 @@ constexpr int HALF_BYTES = TILE_BYTES / 2;
 constexpr int OFF_Q = 0;                        // 2 query tiles
 constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;   // 2 stages
 constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;   // 2 stages
-constexpr int OFF_BAR = OFF_V + 2 * TILE_BYTES;
+constexpr int OFF_MASK = OFF_V + 2 * TILE_BYTES;
+constexpr int kMaskWords = 2048;  // key-validity bitmask held in shared memory: up to 65536 keys
+constexpr int OFF_BAR = OFF_MASK + kMaskWords * 4;
 constexpr int SMEM_TOTAL = OFF_BAR + 256 + 1024;
 
 constexpr uint32_t TM_S = 0;    // S_i at TM_S + 128 i (P_i in its first 64 columns)
@@ -47,7 +49,7 @@ constexpr float kRescaleLog2 = 8.0f;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnArgs p) {
   extern __shared__ uint8_t smem_raw[];
@@ -228,6 +230,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = neg_inf();  // reference max (base-2 units) the exponents are taken against
     float l_run = 0.0f;
     bool ok = true;
+    // key validity (tail and key mask) as a bitmask in shared memory, built once by the 8 softmax
+    // warps: bit k of word w says whether key 32 w + k may be attended
+    uint32_t* mask_words = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
+    const int n_words = n_kv * 4;
+    const bool smem_mask = n_words <= kMaskWords;
+    if (smem_mask) {
+      for (int w = warp - 2; w < n_words; w += 8) {
+        const int kc = w * 32 + lane;
+        bool valid = kc < S;
+        if (valid && p.key_mask != nullptr) valid = p.key_mask[(size_t)b * S + kc] != 0;
+        const uint32_t word = __ballot_sync(0xffffffffu, valid);
+        if (lane == 0) mask_words[w] = word;
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // the 8 softmax warps only
+    }
     for (int j = 0; j < n_kv; ++j) {
       if (!mbar_wait_warp(&s_full[wg], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 8)) {
         ok = false;
@@ -238,10 +255,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr + c * 32);
       tmem_ld_wait();
-      float* s = reinterpret_cast<float*>(sr);
       const int kbase = j * BKV;
-      if (p.key_mask != nullptr || kbase + BKV > S) {
-        uint32_t words[4];
+      uint32_t words[4];
+      if (smem_mask) {
+        const uint4 mw = *reinterpret_cast<const uint4*>(mask_words + j * 4);
+        words[0] = mw.x;
+        words[1] = mw.y;
+        words[2] = mw.z;
+        words[3] = mw.w;
+      } else {
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           const int kc = kbase + w * 32 + lane;
@@ -249,18 +271,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (valid && p.key_mask != nullptr) valid = p.key_mask[(size_t)b * S + kc] != 0;
           words[w] = __ballot_sync(0xffffffffu, valid);
         }
+      }
+      if ((words[0] & words[1] & words[2] & words[3]) != 0xffffffffu) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (!((words[c >> 5] >> (c & 31)) & 1u)) s[c] = neg_inf();
+          if (!((words[c >> 5] >> (c & 31)) & 1u)) sr[c] = 0xff800000u;  // -inf
       }
       // row max and (below) row sum with 8 independent partials: short dependency chains
       float mp[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mp[k] = s[k];
+      for (int k = 0; k < 8; ++k) mp[k] = __uint_as_float(sr[k]);
 #pragma unroll
       for (int c = 8; c < 128; c += 8) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[c + k]);
+        for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], __uint_as_float(sr[c + k]));
       }
       const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                              fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
@@ -273,14 +297,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float m_use = (m_run == neg_inf()) ? 0.0f : m_run;
       float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[64];
+      // P in place: word c of sr receives the bf16 pair (2c, 2c+1), whose scores were read at
+      // step c (ascending c never overwrites a score that is still to be read)
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float e0 = ex2_approx(fmaf(s[2 * c], sl2, -m_use));
-        const float e1 = ex2_approx(fmaf(s[2 * c + 1], sl2, -m_use));
+        const float e0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
+        const float e1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
         sp[(2 * c) & 7] += e0;
         sp[(2 * c + 1) & 7] += e1;
-        pk[c] = pack_bf16x2(e0, e1);
+        sr[c] = pack_bf16x2(e0, e1);
       }
       const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       l_run = l_run * alpha + sum;
@@ -306,8 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // P (bf16) over the first 64 columns of S_i
-      tmem_st32(t_s, pk);
-      tmem_st32(t_s + 32, pk + 32);
+      tmem_st32(t_s, sr);
+      tmem_st32(t_s + 32, sr + 32);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
