@@ -49,7 +49,9 @@ constexpr float kRescaleLog2 = 8.0f;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-__global__ void __maxnreg__(200)
+// 10 warps put 3 warps on two of the four SM sub-partitions, each with 16K registers: at most 168
+// registers per thread, which the launch bound below lets the compiler derive.
+__global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnArgs p) {
   extern __shared__ uint8_t smem_raw[];
