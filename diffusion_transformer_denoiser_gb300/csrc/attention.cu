@@ -11,7 +11,9 @@
 //   * warp 1   : one thread issues, per key tile j, in this order
 //                  O0 += P0 V_j,  S0 = Q0 K_{j+1}^T,  O1 += P1 V_j,  S1 = Q1 K_{j+1}^T
 //                so the tensor core works on one query tile while the softmax works on the other.
-//   * warps 2-5 (query tile 0) and 6-9 (query tile 1): one thread per query row.  Scores come
+//   * warps 2-3: idle after set-up.  Warps 0-3 form one warpgroup that gives registers away
+//                (setmaxnreg) to the two softmax warpgroups.
+//   * warps 4-7 (query tile 0) and 8-11 (query tile 1): one thread per query row.  Scores come
 //                from TMEM; the key tail and masked keys become -inf; the running max lives in
 //                base 2 with log2(e)/sqrt(128) folded into one FMA; P is rounded to bf16 and
 //                written back into TMEM over the scores, where it is the A operand of P V.  O is
@@ -22,6 +24,7 @@
 // issued right after the P_i(j) V_j product that still reads P_i(j) from the same columns.  Tile
 // order and reduction order are fixed: results repeat bit for bit.
 #include "mi_internal.h"
+#include "exp2_poly.h"
 #include "ptx.cuh"
 
 namespace mi {
@@ -30,7 +33,15 @@ namespace {
 
 constexpr int BQ = 128;
 constexpr int BKV = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+// Register split (setmaxnreg): the kernel launches with 168 registers per thread (384 threads);
+// warpgroup 0 (producer, MMA, 2 idle warps) drops to 104 and the two softmax warpgroups rise to
+// 192: 128 * 104 + 256 * 192 = 62464 <= 384 * 168 = 64512, and each SM sub-partition holds one
+// warp of each warpgroup: 104 + 192 + 192 <= 512 registers per lane.  The launcher checks the
+// compiled register count against this split before the first launch (an increase that the pool
+// cannot cover would wait forever).
+constexpr int kRegsLow = 104;
+constexpr int kRegsHigh = 192;
 constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128 x 128 bf16 tile = two 16 KB swizzled halves
 constexpr int HALF_BYTES = TILE_BYTES / 2;
 
@@ -46,11 +57,34 @@ constexpr uint32_t TM_S = 0;    // S_i at TM_S + 128 i (P_i in its first 64 colu
 constexpr uint32_t TM_O = 256;  // O_i at TM_O + 128 i
 constexpr uint32_t TM_COLS = 512;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kPolyPer8 = 3;  // pairs of every 8 whose exponential runs on the FMA pipe
+
+// 2^x for both halves of x2 on the FMA pipe: x = n + f with n = rint(x) (1.5 * 2^23 rounds to an
+// integer; exact for |x| < 2^22), 2^f by the degree-3 minimax polynomial of exp2_poly.h, and 2^n
+// added into the exponent field (the integer n sits in the low mantissa bits of t, so t << 23 is
+// n << 23).  Inputs are clamped at -125 so the result stays a normal float; a softmax term that
+// small is below the fp32 resolution of the row sum.
+__device__ __forceinline__ void exp2_poly2(f32x2_t x2, float& r0, float& r1) {
+  float x0, x1;
+  f2_unpack(x2, x0, x1);
+  x2 = f2_pack(fmaxf(x0, -125.0f), fmaxf(x1, -125.0f));
+  const f32x2_t magic = f2_pack(12582912.0f, 12582912.0f);
+  const f32x2_t neg_magic = f2_pack(-12582912.0f, -12582912.0f);
+  const f32x2_t t = f2_add(x2, magic);
+  const f32x2_t n = f2_add(t, neg_magic);
+  const f32x2_t f = f2_fma(n, f2_pack(-1.0f, -1.0f), x2);  // x - n, exact
+  f32x2_t p = f2_fma(f2_pack(MI_EXP2_C3, MI_EXP2_C3), f, f2_pack(MI_EXP2_C2, MI_EXP2_C2));
+  p = f2_fma(p, f, f2_pack(MI_EXP2_C1, MI_EXP2_C1));
+  p = f2_fma(p, f, f2_pack(MI_EXP2_C0, MI_EXP2_C0));
+  float t0, t1, p0, p1;
+  f2_unpack(t, t0, t1);
+  f2_unpack(p, p0, p1);
+  r0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
+  r1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
+}
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-// 10 warps put 3 warps on two of the four SM sub-partitions, each with 16K registers: at most 168
-// registers per thread, which the launch bound below lets the compiler derive.
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnArgs p) {
@@ -105,6 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------------ TMA producer
@@ -220,9 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(drain);
       mbar_wait_drain(drain, 0, p.err, DEV_TIMEOUT_ATTN + 7);
     }
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     // ------------------------------------------------------------------ softmax / epilogue
-    const int wg = (warp - 2) >> 2;  // query tile of this warpgroup
+    const int wg = (warp - 4) >> 2;  // query tile of this warpgroup
     const int qw = warp & 3;         // TMEM lane quarter of this warp
     const int r = qw * 32 + lane;    // query row inside the tile == TMEM lane
     const uint32_t t_lane = tmem_base + ((uint32_t)(qw * 32) << 16);
@@ -238,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_words = n_kv * 4;
     const bool smem_mask = n_words <= kMaskWords;
     if (smem_mask) {
-      for (int w = warp - 2; w < n_words; w += 8) {
+      for (int w = warp - 4; w < n_words; w += 8) {
         const int kc = w * 32 + lane;
         bool valid = kc < S;
         if (valid && p.key_mask != nullptr) valid = p.key_mask[(size_t)b * S + kc] != 0;
@@ -253,10 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sr[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr + c * 32);
-      tmem_ld_wait();
+      // pass 1: the row max (scores of masked keys and of the key tail count as -inf)
       const int kbase = j * BKV;
       uint32_t words[4];
       if (smem_mask) {
@@ -274,22 +309,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           words[w] = __ballot_sync(0xffffffffu, valid);
         }
       }
-      if ((words[0] & words[1] & words[2] & words[3]) != 0xffffffffu) {
+      const bool full_tile = (words[0] & words[1] & words[2] & words[3]) == 0xffffffffu;
+      float mx;
+      {
+        uint32_t sr[128];
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (!((words[c >> 5] >> (c & 31)) & 1u)) sr[c] = 0xff800000u;  // -inf
+        for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr + c * 32);
+        tmem_ld_wait();
+        if (!full_tile) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (!((words[c >> 5] >> (c & 31)) & 1u)) sr[c] = 0xff800000u;  // -inf
+        }
+        // 3-input max over 8 independent partials (short dependency chains)
+        float mp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mp[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[8 + k]));
+#pragma unroll
+        for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mp[k] = fmax3(mp[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+        }
+        mx = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
       }
-      // row max and (below) row sum with 8 independent partials: short dependency chains
-      float mp[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mp[k] = __uint_as_float(sr[k]);
-#pragma unroll
-      for (int c = 8; c < 128; c += 8) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], __uint_as_float(sr[c + k]));
-      }
-      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       const float m_cand = mx * sl2;
       float alpha = 1.0f;
       const bool grow = m_cand > m_run + kRescaleLog2;  // also true for the first finite max
@@ -298,18 +341,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = m_cand;
       }
       const float m_use = (m_run == neg_inf()) ? 0.0f : m_run;
-      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      // P in place: word c of sr receives the bf16 pair (2c, 2c+1), whose scores were read at
-      // step c (ascending c never overwrites a score that is still to be read)
+      const f32x2_t sl2x2 = f2_pack(sl2, sl2);
+      const f32x2_t negm2 = f2_pack(-m_use, -m_use);
+      f32x2_t sp[4] = {0ull, 0ull, 0ull, 0ull};
+      // pass 2: the scores again, 32 columns at a time (the next chunk's load overlaps this
+      // chunk's exponentials).  x = s log2(e)/sqrt(d) - m in packed pairs; chunk c's 16 packed bf16
+      // words of P go to columns [16c, 16c + 16), which hold scores of chunk c/2, already read.
+      // On tiles without masked keys kPolyPer8 of every 8 pairs take the polynomial exponential on
+      // the FMA pipe and the rest the MUFU ex2, so the two pipes share the tile.
+      uint32_t cbuf[2][32];
+      tmem_ld32(t_s, cbuf[0]);
+      tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float e0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
-        const float e1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
-        sp[(2 * c) & 7] += e0;
-        sp[(2 * c + 1) & 7] += e1;
-        sr[c] = pack_bf16x2(e0, e1);
+      for (int c = 0; c < 4; ++c) {
+        if (c < 3) tmem_ld32(t_s + (c + 1) * 32, cbuf[(c + 1) & 1]);
+        const uint32_t* cs = cbuf[c & 1];
+        uint32_t pw[16];
+        if (full_tile) {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const f32x2_t x2 = f2_fma(f2_pack(__uint_as_float(cs[2 * q]), __uint_as_float(cs[2 * q + 1])), sl2x2, negm2);
+            float e0, e1;
+            if ((q & 7) < kPolyPer8) {
+              exp2_poly2(x2, e0, e1);
+            } else {
+              float x0, x1;
+              f2_unpack(x2, x0, x1);
+              e0 = ex2_approx(x0);
+              e1 = ex2_approx(x1);
+            }
+            sp[q & 3] = f2_add(sp[q & 3], f2_pack(e0, e1));
+            pw[q] = pack_bf16x2(e0, e1);
+          }
+        } else {
+          const uint32_t wbits = words[c];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float s0 = ((wbits >> (2 * q)) & 1u) ? __uint_as_float(cs[2 * q]) : neg_inf();
+            const float s1 = ((wbits >> (2 * q + 1)) & 1u) ? __uint_as_float(cs[2 * q + 1]) : neg_inf();
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s0, s1), sl2x2, negm2), x0, x1);
+            const float e0 = ex2_approx(x0);  // masked keys: ex2(-inf) = 0 exactly
+            const float e1 = ex2_approx(x1);
+            sp[q & 3] = f2_add(sp[q & 3], f2_pack(e0, e1));
+            pw[q] = pack_bf16x2(e0, e1);
+          }
+        }
+        tmem_st16(t_s + c * 16, pw);
+        if (c < 3) tmem_ld_wait();
       }
-      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      float s0, s1, s2, s3, s4, s5, s6, s7;
+      f2_unpack(sp[0], s0, s1);
+      f2_unpack(sp[1], s2, s3);
+      f2_unpack(sp[2], s4, s5);
+      f2_unpack(sp[3], s6, s7);
+      const float sum = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
       l_run = l_run * alpha + sum;
 
       if (j > 0) {
@@ -332,9 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // P (bf16) over the first 64 columns of S_i
-      tmem_st32(t_s, sr);
-      tmem_st32(t_s + 32, sr + 32);
+      // P (stored chunk by chunk above) must have landed before the MMA may read it
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -385,6 +469,12 @@ cudaError_t attention_launch(const CUtensorMap& tq, const CUtensorMap& tk, const
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!attr_done[dev]) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * kThreads < 128 * kRegsLow + 256 * kRegsHigh || fa.numRegs > kRegsHigh ||
+        fa.numRegs < kRegsLow)
+      return cudaErrorInvalidConfiguration;  // the register split would not be covered
     e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
