@@ -33,15 +33,15 @@ namespace {
 
 constexpr int BQ = 128;
 constexpr int BKV = 128;
-constexpr int kThreads = 384;
-// Register split (setmaxnreg): the kernel launches with 168 registers per thread (384 threads);
-// warpgroup 0 (producer, MMA, 2 idle warps) drops to 104 and the two softmax warpgroups rise to
-// 192: 128 * 104 + 256 * 192 = 62464 <= 384 * 168 = 64512, and each SM sub-partition holds one
-// warp of each warpgroup: 104 + 192 + 192 <= 512 registers per lane.  The launcher checks the
-// compiled register count against this split before the first launch (an increase that the pool
-// cannot cover would wait forever).
-constexpr int kRegsLow = 104;
-constexpr int kRegsHigh = 192;
+constexpr int kThreads = 640;
+// Register split (setmaxnreg): the kernel launches with 96 registers per thread (640 threads);
+// warpgroup 0 (producer, MMA, 2 idle warps) drops to 56 and the four softmax warpgroups rise to
+// 104: 128 * 56 + 512 * 104 = 60416 <= 640 * 96 = 61440, and each SM sub-partition holds one warp
+// of each warpgroup: 56 + 4 * 104 <= 512 registers per lane.  The launcher checks the compiled
+// register count against this split before the first launch (an increase that the pool cannot
+// cover would wait forever).
+constexpr int kRegsLow = 56;
+constexpr int kRegsHigh = 104;
 constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128 x 128 bf16 tile = two 16 KB swizzled halves
 constexpr int HALF_BYTES = TILE_BYTES / 2;
 
@@ -50,8 +50,10 @@ constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;   // 2 stages
 constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;   // 2 stages
 constexpr int OFF_MASK = OFF_V + 2 * TILE_BYTES;
 constexpr int kMaskWords = 2048;  // key-validity bitmask held in shared memory: up to 65536 keys
-constexpr int OFF_BAR = OFF_MASK + kMaskWords * 4;
-constexpr int SMEM_TOTAL = OFF_BAR + 256 + 1024;
+constexpr int OFF_XCH = OFF_MASK + kMaskWords * 4;  // row max / row sum exchange between halves
+constexpr int XCH_FLOATS = 2 * 2 * 2 * 128 + 2 * 2 * 128;
+constexpr int OFF_BAR = OFF_XCH + XCH_FLOATS * 4;
+constexpr int SMEM_TOTAL = OFF_BAR + 512 + 1024;
 
 constexpr uint32_t TM_S = 0;    // S_i at TM_S + 128 i (P_i in its first 64 columns)
 constexpr uint32_t TM_O = 256;  // O_i at TM_O + 128 i
@@ -103,7 +105,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = bars + 11;   // [2] per query tile
   uint64_t* o_done = bars + 13;   // [2] per query tile
   uint64_t* drain = bars + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* xbar = bars + 16;     // [2 tile][2 parity] row-max exchange between row halves
+  uint64_t* lbar = bars + 20;     // [2 tile] row-sum exchange
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -123,10 +127,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&p_full[i], 8);
       mbar_init(&o_done[i], 1);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 8);
+    for (int i = 0; i < 2; ++i) mbar_init(&lbar[i], 8);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -260,79 +266,92 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     // ------------------------------------------------------------------ softmax / epilogue
-    const int wg = (warp - 4) >> 2;  // query tile of this warpgroup
-    const int qw = warp & 3;         // TMEM lane quarter of this warp
-    const int r = qw * 32 + lane;    // query row inside the tile == TMEM lane
+    // Two threads per query row: warpgroup 1 + 2 tile + half (warps 4 + 8 tile + 4 half + q)
+    // takes keys [64 half, 64 half + 64) of every key tile of query tile `tile`.
+    const int sw = warp - 4;              // 0..15
+    const int tile = sw >> 3;             // query tile
+    const int half = (sw >> 2) & 1;       // key half of every key tile
+    const int qw = warp & 3;              // TMEM lane quarter of this warp
+    const int r = qw * 32 + lane;         // query row inside the tile == TMEM lane
     const uint32_t t_lane = tmem_base + ((uint32_t)(qw * 32) << 16);
-    const uint32_t t_s = t_lane + TM_S + (uint32_t)wg * 128u;
-    const uint32_t t_o = t_lane + TM_O + (uint32_t)wg * 128u;
+    const uint32_t t_s = t_lane + TM_S + (uint32_t)tile * 128u;          // scores of this tile
+    const uint32_t t_sh = t_s + (uint32_t)half * 64u;                     // this thread's 64 scores
+    const uint32_t t_ph = t_s + (uint32_t)half * 32u;                     // this thread's 32 P words
+    const uint32_t t_oh = t_lane + TM_O + (uint32_t)tile * 128u + (uint32_t)half * 64u;
+    float* xch = reinterpret_cast<float*>(smem + OFF_XCH);  // [2 parity][2 tile][2 half][128 rows]
     const float sl2 = p.scale_log2;
     float m_run = neg_inf();  // reference max (base-2 units) the exponents are taken against
-    float l_run = 0.0f;
+    float l_run = 0.0f;       // this thread's partial row sum over its key halves
     bool ok = true;
-    // key validity (tail and key mask) as a bitmask in shared memory, built once by the 8 softmax
-    // warps: bit k of word w says whether key 32 w + k may be attended
+    // key validity (tail and key mask) as a bitmask in shared memory, built once by the 16
+    // softmax warps: bit k of word w says whether key 32 w + k may be attended
     uint32_t* mask_words = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
     const int n_words = n_kv * 4;
     const bool smem_mask = n_words <= kMaskWords;
     if (smem_mask) {
-      for (int w = warp - 4; w < n_words; w += 8) {
+      for (int w = sw; w < n_words; w += 16) {
         const int kc = w * 32 + lane;
         bool valid = kc < S;
         if (valid && p.key_mask != nullptr) valid = p.key_mask[(size_t)b * S + kc] != 0;
         const uint32_t word = __ballot_sync(0xffffffffu, valid);
         if (lane == 0) mask_words[w] = word;
       }
-      asm volatile("bar.sync 1, 256;" ::: "memory");  // the 8 softmax warps only
+      asm volatile("bar.sync 1, 512;" ::: "memory");  // the 16 softmax warps only
     }
     for (int j = 0; j < n_kv; ++j) {
-      if (!mbar_wait_warp(&s_full[wg], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 8)) {
+      if (!mbar_wait_warp(&s_full[tile], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 8)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // pass 1: the row max (scores of masked keys and of the key tail count as -inf)
-      const int kbase = j * BKV;
-      uint32_t words[4];
+      uint32_t sr[64];
+      tmem_ld32(t_sh, sr);
+      tmem_ld32(t_sh + 32, sr + 32);
+      // validity of this thread's 64 keys (bit c of the pair of words)
+      uint32_t w0, w1;
       if (smem_mask) {
-        const uint4 mw = *reinterpret_cast<const uint4*>(mask_words + j * 4);
-        words[0] = mw.x;
-        words[1] = mw.y;
-        words[2] = mw.z;
-        words[3] = mw.w;
+        const uint2 mw = *reinterpret_cast<const uint2*>(mask_words + j * 4 + half * 2);
+        w0 = mw.x;
+        w1 = mw.y;
       } else {
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int kc = kbase + w * 32 + lane;
-          bool valid = kc < S;
-          if (valid && p.key_mask != nullptr) valid = p.key_mask[(size_t)b * S + kc] != 0;
-          words[w] = __ballot_sync(0xffffffffu, valid);
+        const int kc0 = j * BKV + half * 64 + lane;
+        bool v0 = kc0 < S, v1 = kc0 + 32 < S;
+        if (p.key_mask != nullptr) {
+          if (v0) v0 = p.key_mask[(size_t)b * S + kc0] != 0;
+          if (v1) v1 = p.key_mask[(size_t)b * S + kc0 + 32] != 0;
         }
+        w0 = __ballot_sync(0xffffffffu, v0);
+        w1 = __ballot_sync(0xffffffffu, v1);
       }
-      const bool full_tile = (words[0] & words[1] & words[2] & words[3]) == 0xffffffffu;
-      float mx;
-      {
-        uint32_t sr[128];
+      const bool full = (w0 & w1) == 0xffffffffu;
+      tmem_ld_wait();
+      if (!full) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr + c * 32);
-        tmem_ld_wait();
-        if (!full_tile) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (!((words[c >> 5] >> (c & 31)) & 1u)) sr[c] = 0xff800000u;  // -inf
-        }
-        // 3-input max over 8 independent partials (short dependency chains)
-        float mp[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mp[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[8 + k]));
-#pragma unroll
-        for (int c = 16; c < 128; c += 16) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mp[k] = fmax3(mp[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
-        }
-        mx = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
+        for (int c = 0; c < 64; ++c)
+          if (!(((c < 32 ? w0 : w1) >> (c & 31)) & 1u)) sr[c] = 0xff800000u;  // -inf
       }
+      // partial row max over this thread's 64 keys (8 independent 3-input chains)
+      float mp[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mp[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[8 + k]));
+#pragma unroll
+      for (int c = 16; c < 64; c += 16) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mp[k] = fmax3(mp[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+      }
+      const float mx_half = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
+      // exchange with the other half of the row; after this barrier both halves have read their
+      // scores, so P may overwrite score columns of either half
+      float* xb = xch + (((j & 1) * 2 + tile) * 2) * 128;
+      xb[half * 128 + r] = mx_half;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xbar[tile * 2 + (j & 1)]);
+      if (!mbar_wait_warp(&xbar[tile * 2 + (j & 1)], (j >> 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 11)) {
+        ok = false;
+        break;
+      }
+      const float mx = fmaxf(xb[r], xb[128 + r]);  // same order in both halves: same result
       const float m_cand = mx * sl2;
       float alpha = 1.0f;
       const bool grow = m_cand > m_run + kRescaleLog2;  // also true for the first finite max
@@ -341,99 +360,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = m_cand;
       }
       const float m_use = (m_run == neg_inf()) ? 0.0f : m_run;
-      const f32x2_t sl2x2 = f2_pack(sl2, sl2);
-      const f32x2_t negm2 = f2_pack(-m_use, -m_use);
-      f32x2_t sp[4] = {0ull, 0ull, 0ull, 0ull};
-      // pass 2: the scores again, 32 columns at a time (the next chunk's load overlaps this
-      // chunk's exponentials).  x = s log2(e)/sqrt(d) - m in packed pairs; chunk c's 16 packed bf16
-      // words of P go to columns [16c, 16c + 16), which hold scores of chunk c/2, already read.
-      // On tiles without masked keys kPolyPer8 of every 8 pairs take the polynomial exponential on
-      // the FMA pipe and the rest the MUFU ex2, so the two pipes share the tile.
-      uint32_t cbuf[2][32];
-      tmem_ld32(t_s, cbuf[0]);
-      tmem_ld_wait();
+      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // P in place: word c of sr receives the bf16 pair (2c, 2c+1), whose scores were read at
+      // step c (ascending c never overwrites a score that is still to be read)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (c < 3) tmem_ld32(t_s + (c + 1) * 32, cbuf[(c + 1) & 1]);
-        const uint32_t* cs = cbuf[c & 1];
-        uint32_t pw[16];
-        if (full_tile) {
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const f32x2_t x2 = f2_fma(f2_pack(__uint_as_float(cs[2 * q]), __uint_as_float(cs[2 * q + 1])), sl2x2, negm2);
-            float e0, e1;
-            if ((q & 7) < kPolyPer8) {
-              exp2_poly2(x2, e0, e1);
-            } else {
-              float x0, x1;
-              f2_unpack(x2, x0, x1);
-              e0 = ex2_approx(x0);
-              e1 = ex2_approx(x1);
-            }
-            sp[q & 3] = f2_add(sp[q & 3], f2_pack(e0, e1));
-            pw[q] = pack_bf16x2(e0, e1);
-          }
-        } else {
-          const uint32_t wbits = words[c];
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const float s0 = ((wbits >> (2 * q)) & 1u) ? __uint_as_float(cs[2 * q]) : neg_inf();
-            const float s1 = ((wbits >> (2 * q + 1)) & 1u) ? __uint_as_float(cs[2 * q + 1]) : neg_inf();
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(s0, s1), sl2x2, negm2), x0, x1);
-            const float e0 = ex2_approx(x0);  // masked keys: ex2(-inf) = 0 exactly
-            const float e1 = ex2_approx(x1);
-            sp[q & 3] = f2_add(sp[q & 3], f2_pack(e0, e1));
-            pw[q] = pack_bf16x2(e0, e1);
-          }
-        }
-        tmem_st16(t_s + c * 16, pw);
-        if (c < 3) tmem_ld_wait();
+      for (int c = 0; c < 32; ++c) {
+        const float e0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));  // ex2(-inf) = 0
+        const float e1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
+        sp[(2 * c) & 7] += e0;
+        sp[(2 * c + 1) & 7] += e1;
+        sr[c] = pack_bf16x2(e0, e1);
       }
-      float s0, s1, s2, s3, s4, s5, s6, s7;
-      f2_unpack(sp[0], s0, s1);
-      f2_unpack(sp[1], s2, s3);
-      f2_unpack(sp[2], s4, s5);
-      f2_unpack(sp[3], s6, s7);
-      const float sum = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       l_run = l_run * alpha + sum;
 
       if (j > 0) {
-        // the previous P V product is complete (S_i(j) was issued after it); keep the phases of
+        // the previous P V product is complete (S(j) was issued after it); keep the phases of
         // o_done in step with the loop
-        if (!mbar_wait_warp(&o_done[wg], (j - 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 9)) {
+        if (!mbar_wait_warp(&o_done[tile], (j - 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 9)) {
           ok = false;
           break;
         }
         tc_fence_after();
         if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
-            tmem_ld32(t_o + c * 32, o);
+            tmem_ld32(t_oh + c * 32, o);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(t_o + c * 32, o);
+            tmem_st32(t_oh + c * 32, o);
           }
         }
       }
-      // P (stored chunk by chunk above) must have landed before the MMA may read it
+      // P (bf16) of this thread's 64 keys: 32 packed columns of the tile's P
+      tmem_st32(t_ph, sr);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[wg]);
+      if (lane == 0) mbar_arrive(&p_full[tile]);
     }
-    if (ok && mbar_wait_warp(&o_done[wg], (n_kv - 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 10)) {
+    if (ok && mbar_wait_warp(&o_done[tile], (n_kv - 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 10)) {
       tc_fence_after();
-      const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
-      const int row = q0 + wg * BQ + r;
+      // the row sum is the sum of the two halves' partial sums (the same order in both halves)
+      float* xl = xch + (2 * 2 * 2 * 128) + (tile * 2) * 128;
+      xl[half * 128 + r] = l_run;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&lbar[tile]);
+      const bool l_ok = mbar_wait_warp(&lbar[tile], 0, abort_flag, p.err, DEV_TIMEOUT_ATTN + 12);
+      const float l_row = l_ok ? xl[r] + xl[128 + r] : 0.0f;
+      const float inv = l_row > 0.0f ? 1.0f / l_row : 0.0f;
+      const int row = q0 + tile * BQ + r;
       const int H = p.n_heads * kHeadDim;
-      __nv_bfloat16* dst_row = p.out + ((size_t)b * S + row) * H + (size_t)h * kHeadDim;
+      __nv_bfloat16* dst_row = p.out + ((size_t)b * S + row) * H + (size_t)h * kHeadDim + half * 64;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        tmem_ld32(t_o + c * 32, o);
+        tmem_ld32(t_oh + c * 32, o);
         tmem_ld_wait();
         if (row < S) {
           uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
@@ -472,7 +456,7 @@ cudaError_t attention_launch(const CUtensorMap& tq, const CUtensorMap& tk, const
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, attn_fwd_kernel);
     if (e != cudaSuccess) return e;
-    if (fa.numRegs * kThreads < 128 * kRegsLow + 256 * kRegsHigh || fa.numRegs > kRegsHigh ||
+    if (fa.numRegs * kThreads < 128 * kRegsLow + 512 * kRegsHigh || fa.numRegs > kRegsHigh ||
         fa.numRegs < kRegsLow)
       return cudaErrorInvalidConfiguration;  // the register split would not be covered
     e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
