@@ -11,9 +11,7 @@
 //   * warp 1   : one thread issues, per key tile j, in this order
 //                  O0 += P0 V_j,  S0 = Q0 K_{j+1}^T,  O1 += P1 V_j,  S1 = Q1 K_{j+1}^T
 //                so the tensor core works on one query tile while the softmax works on the other.
-//   * warps 2-3: idle after set-up.  Warps 0-3 form one warpgroup that gives registers away
-//                (setmaxnreg) to the two softmax warpgroups.
-//   * warps 4-7 (query tile 0) and 8-11 (query tile 1): one thread per query row.  Scores come
+//   * warps 2-5 (query tile 0) and 6-9 (query tile 1): one thread per query row.  Scores come
 //                from TMEM; the key tail and masked keys become -inf; the running max lives in
 //                base 2 with log2(e)/sqrt(128) folded into one FMA; P is rounded to bf16 and
 //                written back into TMEM over the scores, where it is the A operand of P V.  O is
@@ -24,7 +22,6 @@
 // issued right after the P_i(j) V_j product that still reads P_i(j) from the same columns.  Tile
 // order and reduction order are fixed: results repeat bit for bit.
 #include "mi_internal.h"
-#include "exp2_poly.h"
 #include "ptx.cuh"
 
 namespace mi {
@@ -33,15 +30,7 @@ namespace {
 
 constexpr int BQ = 128;
 constexpr int BKV = 128;
-constexpr int kThreads = 640;
-// Register split (setmaxnreg): the kernel launches with 96 registers per thread (640 threads);
-// warpgroup 0 (producer, MMA, 2 idle warps) drops to 56 and the four softmax warpgroups rise to
-// 104: 128 * 56 + 512 * 104 = 60416 <= 640 * 96 = 61440, and each SM sub-partition holds one warp
-// of each warpgroup: 56 + 4 * 104 <= 512 registers per lane.  The launcher checks the compiled
-// register count against this split before the first launch (an increase that the pool cannot
-// cover would wait forever).
-constexpr int kRegsLow = 56;
-constexpr int kRegsHigh = 104;
+constexpr int kThreads = 320;
 constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128 x 128 bf16 tile = two 16 KB swizzled halves
 constexpr int HALF_BYTES = TILE_BYTES / 2;
 
@@ -50,43 +39,18 @@ constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;   // 2 stages
 constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;   // 2 stages
 constexpr int OFF_MASK = OFF_V + 2 * TILE_BYTES;
 constexpr int kMaskWords = 2048;  // key-validity bitmask held in shared memory: up to 65536 keys
-constexpr int OFF_XCH = OFF_MASK + kMaskWords * 4;  // row max / row sum exchange between halves
-constexpr int XCH_FLOATS = 2 * 2 * 2 * 128 + 2 * 2 * 128;
-constexpr int OFF_BAR = OFF_XCH + XCH_FLOATS * 4;
-constexpr int SMEM_TOTAL = OFF_BAR + 512 + 1024;
+constexpr int OFF_BAR = OFF_MASK + kMaskWords * 4;
+constexpr int SMEM_TOTAL = OFF_BAR + 256 + 1024;
 
 constexpr uint32_t TM_S = 0;    // S_i at TM_S + 128 i (P_i in its first 64 columns)
 constexpr uint32_t TM_O = 256;  // O_i at TM_O + 128 i
 constexpr uint32_t TM_COLS = 512;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kPolyPer8 = 3;  // pairs of every 8 whose exponential runs on the FMA pipe
-
-// 2^x for both halves of x2 on the FMA pipe: x = n + f with n = rint(x) (1.5 * 2^23 rounds to an
-// integer; exact for |x| < 2^22), 2^f by the degree-3 minimax polynomial of exp2_poly.h, and 2^n
-// added into the exponent field (the integer n sits in the low mantissa bits of t, so t << 23 is
-// n << 23).  Inputs are clamped at -125 so the result stays a normal float; a softmax term that
-// small is below the fp32 resolution of the row sum.
-__device__ __forceinline__ void exp2_poly2(f32x2_t x2, float& r0, float& r1) {
-  float x0, x1;
-  f2_unpack(x2, x0, x1);
-  x2 = f2_pack(fmaxf(x0, -125.0f), fmaxf(x1, -125.0f));
-  const f32x2_t magic = f2_pack(12582912.0f, 12582912.0f);
-  const f32x2_t neg_magic = f2_pack(-12582912.0f, -12582912.0f);
-  const f32x2_t t = f2_add(x2, magic);
-  const f32x2_t n = f2_add(t, neg_magic);
-  const f32x2_t f = f2_fma(n, f2_pack(-1.0f, -1.0f), x2);  // x - n, exact
-  f32x2_t p = f2_fma(f2_pack(MI_EXP2_C3, MI_EXP2_C3), f, f2_pack(MI_EXP2_C2, MI_EXP2_C2));
-  p = f2_fma(p, f, f2_pack(MI_EXP2_C1, MI_EXP2_C1));
-  p = f2_fma(p, f, f2_pack(MI_EXP2_C0, MI_EXP2_C0));
-  float t0, t1, p0, p1;
-  f2_unpack(t, t0, t1);
-  f2_unpack(p, p0, p1);
-  r0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
-  r1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
-}
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
+// 10 warps put 3 warps on two of the four SM sub-partitions, each with 16K registers: at most 168
+// registers per thread, which the launch bound below lets the compiler derive.
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnArgs p) {
@@ -105,9 +69,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = bars + 11;   // [2] per query tile
   uint64_t* o_done = bars + 13;   // [2] per query tile
   uint64_t* drain = bars + 15;
-  uint64_t* xbar = bars + 16;     // [2 tile][2 parity] row-max exchange between row halves
-  uint64_t* lbar = bars + 20;     // [2 tile] row-sum exchange
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -127,12 +89,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 8);
+      mbar_init(&p_full[i], 4);
       mbar_init(&o_done[i], 1);
     }
     mbar_init(drain, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 8);
-    for (int i = 0; i < 2; ++i) mbar_init(&lbar[i], 8);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -145,8 +105,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------------ TMA producer
@@ -262,96 +220,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(drain);
       mbar_wait_drain(drain, 0, p.err, DEV_TIMEOUT_ATTN + 7);
     }
-  }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     // ------------------------------------------------------------------ softmax / epilogue
-    // Two threads per query row: warpgroup 1 + 2 tile + half (warps 4 + 8 tile + 4 half + q)
-    // takes keys [64 half, 64 half + 64) of every key tile of query tile `tile`.
-    const int sw = warp - 4;              // 0..15
-    const int tile = sw >> 3;             // query tile
-    const int half = (sw >> 2) & 1;       // key half of every key tile
-    const int qw = warp & 3;              // TMEM lane quarter of this warp
-    const int r = qw * 32 + lane;         // query row inside the tile == TMEM lane
+    const int wg = (warp - 2) >> 2;  // query tile of this warpgroup
+    const int qw = warp & 3;         // TMEM lane quarter of this warp
+    const int r = qw * 32 + lane;    // query row inside the tile == TMEM lane
     const uint32_t t_lane = tmem_base + ((uint32_t)(qw * 32) << 16);
-    const uint32_t t_s = t_lane + TM_S + (uint32_t)tile * 128u;          // scores of this tile
-    const uint32_t t_sh = t_s + (uint32_t)half * 64u;                     // this thread's 64 scores
-    const uint32_t t_ph = t_s + (uint32_t)half * 32u;                     // this thread's 32 P words
-    const uint32_t t_oh = t_lane + TM_O + (uint32_t)tile * 128u + (uint32_t)half * 64u;
-    float* xch = reinterpret_cast<float*>(smem + OFF_XCH);  // [2 parity][2 tile][2 half][128 rows]
+    const uint32_t t_s = t_lane + TM_S + (uint32_t)wg * 128u;
+    const uint32_t t_o = t_lane + TM_O + (uint32_t)wg * 128u;
     const float sl2 = p.scale_log2;
     float m_run = neg_inf();  // reference max (base-2 units) the exponents are taken against
-    float l_run = 0.0f;       // this thread's partial row sum over its key halves
+    float l_run = 0.0f;
     bool ok = true;
-    // key validity (tail and key mask) as a bitmask in shared memory, built once by the 16
-    // softmax warps: bit k of word w says whether key 32 w + k may be attended
+    // key validity (tail and key mask) as a bitmask in shared memory, built once by the 8 softmax
+    // warps: bit k of word w says whether key 32 w + k may be attended
     uint32_t* mask_words = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
     const int n_words = n_kv * 4;
     const bool smem_mask = n_words <= kMaskWords;
     if (smem_mask) {
-      for (int w = sw; w < n_words; w += 16) {
+      for (int w = warp - 2; w < n_words; w += 8) {
         const int kc = w * 32 + lane;
         bool valid = kc < S;
         if (valid && p.key_mask != nullptr) valid = p.key_mask[(size_t)b * S + kc] != 0;
         const uint32_t word = __ballot_sync(0xffffffffu, valid);
         if (lane == 0) mask_words[w] = word;
       }
-      asm volatile("bar.sync 1, 512;" ::: "memory");  // the 16 softmax warps only
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // the 8 softmax warps only
     }
     for (int j = 0; j < n_kv; ++j) {
-      if (!mbar_wait_warp(&s_full[tile], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 8)) {
+      if (!mbar_wait_warp(&s_full[wg], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 8)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld32(t_sh, sr);
-      tmem_ld32(t_sh + 32, sr + 32);
-      // validity of this thread's 64 keys (bit c of the pair of words)
-      uint32_t w0, w1;
-      if (smem_mask) {
-        const uint2 mw = *reinterpret_cast<const uint2*>(mask_words + j * 4 + half * 2);
-        w0 = mw.x;
-        w1 = mw.y;
-      } else {
-        const int kc0 = j * BKV + half * 64 + lane;
-        bool v0 = kc0 < S, v1 = kc0 + 32 < S;
-        if (p.key_mask != nullptr) {
-          if (v0) v0 = p.key_mask[(size_t)b * S + kc0] != 0;
-          if (v1) v1 = p.key_mask[(size_t)b * S + kc0 + 32] != 0;
-        }
-        w0 = __ballot_sync(0xffffffffu, v0);
-        w1 = __ballot_sync(0xffffffffu, v1);
-      }
-      const bool full = (w0 & w1) == 0xffffffffu;
-      tmem_ld_wait();
-      if (!full) {
+      uint32_t sr[128];
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (!(((c < 32 ? w0 : w1) >> (c & 31)) & 1u)) sr[c] = 0xff800000u;  // -inf
+      for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr + c * 32);
+      tmem_ld_wait();
+      const int kbase = j * BKV;
+      uint32_t words[4];
+      if (smem_mask) {
+        const uint4 mw = *reinterpret_cast<const uint4*>(mask_words + j * 4);
+        words[0] = mw.x;
+        words[1] = mw.y;
+        words[2] = mw.z;
+        words[3] = mw.w;
+      } else {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int kc = kbase + w * 32 + lane;
+          bool valid = kc < S;
+          if (valid && p.key_mask != nullptr) valid = p.key_mask[(size_t)b * S + kc] != 0;
+          words[w] = __ballot_sync(0xffffffffu, valid);
+        }
       }
-      // partial row max over this thread's 64 keys (8 independent 3-input chains)
+      if ((words[0] & words[1] & words[2] & words[3]) != 0xffffffffu) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (!((words[c >> 5] >> (c & 31)) & 1u)) sr[c] = 0xff800000u;  // -inf
+      }
+      // row max and (below) row sum with 8 independent partials: short dependency chains
       float mp[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mp[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[8 + k]));
+      for (int k = 0; k < 8; ++k) mp[k] = __uint_as_float(sr[k]);
 #pragma unroll
-      for (int c = 16; c < 64; c += 16) {
+      for (int c = 8; c < 128; c += 8) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mp[k] = fmax3(mp[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+        for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], __uint_as_float(sr[c + k]));
       }
-      const float mx_half = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
-      // exchange with the other half of the row; after this barrier both halves have read their
-      // scores, so P may overwrite score columns of either half
-      float* xb = xch + (((j & 1) * 2 + tile) * 2) * 128;
-      xb[half * 128 + r] = mx_half;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&xbar[tile * 2 + (j & 1)]);
-      if (!mbar_wait_warp(&xbar[tile * 2 + (j & 1)], (j >> 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 11)) {
-        ok = false;
-        break;
-      }
-      const float mx = fmaxf(xb[r], xb[128 + r]);  // same order in both halves: same result
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       const float m_cand = mx * sl2;
       float alpha = 1.0f;
       const bool grow = m_cand > m_run + kRescaleLog2;  // also true for the first finite max
@@ -364,8 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P in place: word c of sr receives the bf16 pair (2c, 2c+1), whose scores were read at
       // step c (ascending c never overwrites a score that is still to be read)
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float e0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));  // ex2(-inf) = 0
+      for (int c = 0; c < 64; ++c) {
+        const float e0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
         const float e1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
         sp[(2 * c) & 7] += e0;
         sp[(2 * c + 1) & 7] += e1;
@@ -375,49 +313,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_run = l_run * alpha + sum;
 
       if (j > 0) {
-        // the previous P V product is complete (S(j) was issued after it); keep the phases of
+        // the previous P V product is complete (S_i(j) was issued after it); keep the phases of
         // o_done in step with the loop
-        if (!mbar_wait_warp(&o_done[tile], (j - 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 9)) {
+        if (!mbar_wait_warp(&o_done[wg], (j - 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 9)) {
           ok = false;
           break;
         }
         tc_fence_after();
         if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
-            tmem_ld32(t_oh + c * 32, o);
+            tmem_ld32(t_o + c * 32, o);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(t_oh + c * 32, o);
+            tmem_st32(t_o + c * 32, o);
           }
         }
       }
-      // P (bf16) of this thread's 64 keys: 32 packed columns of the tile's P
-      tmem_st32(t_ph, sr);
+      // P (bf16) over the first 64 columns of S_i
+      tmem_st32(t_s, sr);
+      tmem_st32(t_s + 32, sr + 32);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[tile]);
+      if (lane == 0) mbar_arrive(&p_full[wg]);
     }
-    if (ok && mbar_wait_warp(&o_done[tile], (n_kv - 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 10)) {
+    if (ok && mbar_wait_warp(&o_done[wg], (n_kv - 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 10)) {
       tc_fence_after();
-      // the row sum is the sum of the two halves' partial sums (the same order in both halves)
-      float* xl = xch + (2 * 2 * 2 * 128) + (tile * 2) * 128;
-      xl[half * 128 + r] = l_run;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&lbar[tile]);
-      const bool l_ok = mbar_wait_warp(&lbar[tile], 0, abort_flag, p.err, DEV_TIMEOUT_ATTN + 12);
-      const float l_row = l_ok ? xl[r] + xl[128 + r] : 0.0f;
-      const float inv = l_row > 0.0f ? 1.0f / l_row : 0.0f;
-      const int row = q0 + tile * BQ + r;
+      const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+      const int row = q0 + wg * BQ + r;
       const int H = p.n_heads * kHeadDim;
-      __nv_bfloat16* dst_row = p.out + ((size_t)b * S + row) * H + (size_t)h * kHeadDim + half * 64;
+      __nv_bfloat16* dst_row = p.out + ((size_t)b * S + row) * H + (size_t)h * kHeadDim;
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
-        tmem_ld32(t_oh + c * 32, o);
+        tmem_ld32(t_o + c * 32, o);
         tmem_ld_wait();
         if (row < S) {
           uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
@@ -453,12 +385,6 @@ cudaError_t attention_launch(const CUtensorMap& tq, const CUtensorMap& tk, const
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!attr_done[dev]) {
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs * kThreads < 128 * kRegsLow + 512 * kRegsHigh || fa.numRegs > kRegsHigh ||
-        fa.numRegs < kRegsLow)
-      return cudaErrorInvalidConfiguration;  // the register split would not be covered
     e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
