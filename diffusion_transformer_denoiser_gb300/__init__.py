@@ -73,6 +73,7 @@ _SIGNATURES = {
     "mi_block_workspace_size": ([_P, _I, _I, ctypes.POINTER(_SZ)], _I),
     "mi_block_tensor_offset": ([_P, _I, _I, _I, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)], _I),
     "mi_block_forward": ([_P, ctypes.POINTER(SeqLayout), _P, _P, _P, _P, _P, _I, _P, _P, _SZ, _P], _I),
+    "mi_block_forward_static_ws": ([_P, ctypes.POINTER(SeqLayout), _P, _P, _P, _P, _P, _I, _P, _P], _I),
     "mi_model_init": ([ctypes.POINTER(_P), ctypes.POINTER(_ModelDesc)], _I),
     "mi_model_destroy": ([_P], None),
     "mi_model_workspace_size": ([_P, ctypes.POINTER(SeqLayout), ctypes.POINTER(_SZ)], _I),

@@ -750,3 +750,50 @@ mi_status mi_silu_gate(const void* gu, void* m, int rows, int inter, void* strea
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------ static workspace
+// A block forward for callers that cannot allocate device memory themselves.  Its workspace is a
+// file-scope device array of fixed size that every GPU loading this library holds until the
+// process exits.  Host code must not use the array's name as a device address; the address is
+// looked up once per device with cudaGetSymbolAddress, with that device current.
+namespace {
+
+constexpr size_t kStaticWsBytes = (size_t)64 << 20;
+static_assert(kStaticWsBytes == MI_STATIC_WS_BYTES, "the header states the static workspace size");
+__device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];
+
+void* g_static_ws_ptr[mi::kMaxDevices] = {};
+std::mutex g_static_ws_mu;
+
+mi_status static_ws_address(void** out) {
+  int dev = 0;
+  MI_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev < 0 || dev >= mi::kMaxDevices) return fail(MI_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_static_ws_mu);
+  if (!g_static_ws_ptr[dev]) {
+    void* p = nullptr;
+    MI_CUDA(cudaGetSymbolAddress(&p, g_static_ws), "cudaGetSymbolAddress(static workspace)");
+    g_static_ws_ptr[dev] = p;
+  }
+  *out = g_static_ws_ptr[dev];
+  return MI_OK;
+}
+
+}  // namespace
+
+extern "C" mi_status mi_block_forward_static_ws(mi_block* blk, const mi_seq_layout* L, const void* x, void* y,
+                                                const void* mod, const float* rope_cos, const float* rope_sin,
+                                                int rope_bstride, const uint8_t* key_mask, void* stream) {
+  if (!blk) return fail(MI_ERR_INVALID_ARG, "null block");
+  int S = 0;
+  mi_status st = check_layout(L, &S);
+  if (st != MI_OK) return st;
+  const size_t need = plan_ws(blk->d, L->batch, S).total;
+  if (need > kStaticWsBytes)
+    return fail(MI_ERR_WORKSPACE, "this geometry needs a %zu-byte workspace; the static one holds %zu bytes", need,
+                kStaticWsBytes);
+  void* ws = nullptr;
+  st = static_ws_address(&ws);
+  if (st != MI_OK) return st;
+  return mi_block_forward(blk, L, x, y, mod, rope_cos, rope_sin, rope_bstride, key_mask, ws, kStaticWsBytes, stream);
+}

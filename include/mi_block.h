@@ -138,6 +138,26 @@ mi_status mi_block_forward(mi_block* blk, const mi_seq_layout* L, const void* x,
                            const float* rope_cos, const float* rope_sin, int rope_bstride,
                            const uint8_t* key_mask, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * mi_block_forward without a caller workspace, for callers that cannot call cudaMalloc: for
+ * example a plugin whose host owns every device allocation through its own pool, or code that
+ * must not allocate after start-up.  The paper has no counterpart: it is an interface addition.
+ *
+ * The workspace is a static device array of MI_STATIC_WS_BYTES inside this library, held by every
+ * GPU that loads the library until the process exits.  Geometries whose mi_block_workspace_size
+ * exceeds it are refused with MI_ERR_WORKSPACE.  Nothing is allocated: no cudaMalloc, cudaFree or
+ * allocating library routine.  The first call on a device looks the array's address up
+ * (cudaGetSymbolAddress, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's contents (the block
+ * overwrites every intermediate before reading it, so nothing needs clearing); calls that overlap
+ * on the GPU (different streams, or different threads without ordering) race on it.  Arguments and
+ * results are exactly those of mi_block_forward.
+ */
+#define MI_STATIC_WS_BYTES ((size_t)64 << 20)
+mi_status mi_block_forward_static_ws(mi_block* blk, const mi_seq_layout* L, const void* x, void* y, const void* mod,
+                                     const float* rope_cos, const float* rope_sin, int rope_bstride,
+                                     const uint8_t* key_mask, void* stream);
+
 /* ------------------------------------------------------------------------- denoising step --- */
 
 typedef struct mi_model_desc {
