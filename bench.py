@@ -220,9 +220,10 @@ def _traffic_for(kernel: str):
     ent = d.get(kernel)
     if not ent:
         return None
-    src = os.path.join(ROOT, ent["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != ent["source_sha256"]:
-        return None
+    for rel, sha in ent["sources"].items():
+        src = os.path.join(ROOT, rel)
+        if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != sha:
+            return None
     return ent["dram_bytes_per_launch"]
 
 

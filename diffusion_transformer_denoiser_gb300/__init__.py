@@ -68,6 +68,7 @@ _SIGNATURES = {
     "mi_abi_version": ([], _I),
     "mi_device_supported": ([], _I),
     "mi_device_error": ([ctypes.POINTER(_I)], _I),
+    "mi_selftest_wait_timeout": ([_I, _P], _I),
     "mi_block_init": ([ctypes.POINTER(_P), ctypes.POINTER(_BlockDesc)], _I),
     "mi_block_destroy": ([_P], None),
     "mi_block_workspace_size": ([_P, _I, _I, ctypes.POINTER(_SZ)], _I),
@@ -142,6 +143,11 @@ def device_error() -> int:
     code = _I(0)
     _check(lib().mi_device_error(ctypes.byref(code)))
     return code.value
+
+
+def selftest_wait_timeout(limit_us: int = 10000, stream=None):
+    """Enqueue the bounded-wait self-test kernel (its wait runs out after limit_us)."""
+    _check(lib().mi_selftest_wait_timeout(limit_us, _stream(stream)))
 
 
 class Block:

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmi_block.so")
-SOURCES = ["api.cu", "gemm.cu", "attention.cu", "elementwise.cu"]
+SOURCES = ["api.cu", "gemm.cu", "attention.cu", "elementwise.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

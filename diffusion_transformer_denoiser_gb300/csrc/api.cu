@@ -387,6 +387,16 @@ mi_status mi_device_error(int* code) {
   return MI_OK;
 }
 
+mi_status mi_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us <= 0 || limit_us > 1000000) return fail(MI_ERR_INVALID_ARG, "limit_us must be in (0, 1e6]");
+  DeviceInfo* dev = nullptr;
+  mi_status st = require_sm103(&dev);
+  if (st != MI_OK) return st;
+  cudaError_t e = mi::wait_timeout_selftest_launch(dev->err, (unsigned long long)limit_us * 1000ull,
+                                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MI_OK : cuda_fail(e, "wait self-test launch");
+}
+
 mi_status mi_block_init(mi_block** out, const mi_block_desc* desc) {
   if (!out) return fail(MI_ERR_INVALID_ARG, "null output pointer");
   *out = nullptr;

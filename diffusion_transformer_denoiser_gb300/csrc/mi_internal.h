@@ -66,7 +66,10 @@ cudaError_t cfg_euler_launch(const float* vel, float* latent, int n_img, int cha
                              int batch, cudaStream_t s);
 cudaError_t f32_to_bf16_launch(const float* src, __nv_bfloat16* dst, size_t n, cudaStream_t s);
 
-// Tensor maps (tmap.cpp).
+// Self-test of the bounded pipeline waits (selftest.cu).
+cudaError_t wait_timeout_selftest_launch(int* err, unsigned long long limit_ns, cudaStream_t s);
+
+// Tensor maps (api.cu).
 bool encode_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
                     uint32_t box_inner, uint32_t box_rows);
 bool encode_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,

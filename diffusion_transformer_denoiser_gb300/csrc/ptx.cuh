@@ -17,11 +17,15 @@ enum : int {
   DEV_OK = 0,
   DEV_TIMEOUT_GEMM = 0x100,
   DEV_TIMEOUT_ATTN = 0x200,
+  DEV_TIMEOUT_SELFTEST = 0x300,
 };
 
 // Wall-clock limit of a single wait (ns).  No legitimate wait in these kernels lasts more than a
 // few milliseconds; the limit only turns a pipeline bug into an error status instead of a hang.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// Backstop on the number of polls of one wait (seconds of polling at any realistic poll rate), so a
+// wait ends even if the global timer were not advancing.
+constexpr uint32_t kWaitPollCap = 1u << 28;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -66,7 +70,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase of `bar` with the given parity to complete.  Returns false (and the caller
 // must stop its pipeline role) when the CTA was aborted or this wait ran past the limit.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err, int code) {
+                                          int* err, int code, unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
@@ -75,7 +79,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(a, parity)) return true;
     if (((++it) & 63u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns || it >= kWaitPollCap) {
         *abort_flag = 1;
         atomicCAS(err, 0, code);
         return false;
@@ -98,8 +102,9 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return;
   const unsigned long long t0 = globaltimer_ns();
+  uint32_t it = 0;
   while (!mbar_try_wait(a, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs || ++it >= kWaitPollCap) {
       atomicCAS(err, 0, code);
       return;
     }

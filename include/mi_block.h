@@ -63,6 +63,17 @@ mi_status mi_device_supported(void);
  * Synchronises the device (diagnostic call, not for the hot path). */
 mi_status mi_device_error(int* code);
 
+/* Error codes mi_device_error reports: 0x100 + k (a GEMM wait), 0x200 + k (an attention wait),
+ * 0x300 (the self-test below). */
+#define MI_DEV_TIMEOUT_GEMM 0x100
+#define MI_DEV_TIMEOUT_ATTN 0x200
+#define MI_DEV_TIMEOUT_SELFTEST 0x300
+
+/* Enqueues a one-CTA kernel whose pipeline wait can never complete: the wait gives up after
+ * limit_us microseconds (at most 1e6), records MI_DEV_TIMEOUT_SELFTEST in the device error flag and
+ * the kernel returns.  Exercises the failure path of the bounded waits without a fault or hang. */
+mi_status mi_selftest_wait_timeout(int limit_us, void* stream);
+
 /* ---------------------------------------------------------------------------------- block --- */
 
 typedef struct mi_block_desc {
