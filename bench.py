@@ -218,7 +218,7 @@ def _traffic_for(kernel: str):
     with open(p) as f:
         d = json.load(f)
     ent = d.get(kernel)
-    if not ent:
+    if not ent or "sources" not in ent:
         return None
     for rel, sha in ent["sources"].items():
         src = os.path.join(ROOT, rel)
