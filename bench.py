@@ -365,7 +365,7 @@ def run_ours(args):
             "cpu_baseline": None,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": xbytes, "d2h_bytes_per_step": xbytes,
                     "ms_per_step": max(e2e_all)},
-            "gpu_launches": args.steps * 8,
+            "gpu_launches": args.steps * 7,
             "clocks": clocks,
             "device_error": err,
         }
@@ -407,8 +407,7 @@ def kernel_times(mi, torch, g, inp, t, devc, stream, reps):
     mask = torch.from_numpy(inp.key_mask).to(devc)
     # realistic operands for each kernel: run the chain once
     mi.mod_rmsnorm(x, mod, 0, 1, h, B, S, g.eps)
-    mi.gemm(h, w_qkv, qkv)
-    mi.qk_norm_rope(qkv, wq, wk, cos, sin, qp, kp, B, S, nh, g.eps)
+    mi.gemm_qkv_rope(h, w_qkv, wq, wk, cos, sin, qp, kp, qkv, B, S, nh, g.eps)
     mi.attention(qp, kp, qkv, mask, o, B, S, nh)
     mi.gemm_gated_residual(o, w_o, x, mod, 2, x1, S)
     mi.gemm_silu_gate(h, w_gu, m)
@@ -416,9 +415,8 @@ def kernel_times(mi, torch, g, inp, t, devc, stream, reps):
     gemm_f, attn_f = flops_of(g)
     calls = {
         "mod_rmsnorm": (lambda: mi.mod_rmsnorm(x, mod, 0, 1, h, B, S, g.eps), {"bytes": 4 * R * H}),
-        "gemm_qkv": (lambda: mi.gemm(h, w_qkv, qkv), {"flops": 2.0 * R * 3 * H * H}),
-        "qk_norm_rope": (lambda: mi.qk_norm_rope(qkv, wq, wk, cos, sin, qp, kp, B, S, nh, g.eps),
-                         {"bytes": 8 * R * H + 512 * R}),
+        "gemm_qkv_rope": (lambda: mi.gemm_qkv_rope(h, w_qkv, wq, wk, cos, sin, qp, kp, qkv, B, S, nh, g.eps),
+                          {"flops": 2.0 * R * 3 * H * H}),
         "attention": (lambda: mi.attention(qp, kp, qkv, mask, o, B, S, nh), {"flops": float(attn_f)}),
         "gemm_out_gated_residual": (lambda: mi.gemm_gated_residual(o, w_o, x, mod, 2, x1, S),
                                     {"flops": 2.0 * R * H * H}),

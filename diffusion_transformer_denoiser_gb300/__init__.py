@@ -15,7 +15,7 @@ import torch
 
 __all__ = [
     "MiError", "lib", "library_path", "Block", "Model", "SeqLayout", "mod_rmsnorm", "gemm",
-    "gemm_gated_residual", "gemm_silu_gate", "qk_norm_rope", "attention", "gated_add", "silu_gate",
+    "gemm_gated_residual", "gemm_silu_gate", "gemm_qkv_rope", "qk_norm_rope", "attention", "gated_add", "silu_gate",
     "device_error", "device_supported", "TENSORS",
 ]
 
@@ -84,6 +84,7 @@ _SIGNATURES = {
     "mi_gemm_bf16": ([_P, _P, _P, _I, _I, _I, _P], _I),
     "mi_gemm_bf16_gated_residual": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
     "mi_gemm_bf16_silu_gate": ([_P, _P, _P, _I, _I, _I, _P], _I),
+    "mi_gemm_bf16_qkv_rope": ([_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P], _I),
     "mi_qk_norm_rope": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _F, _P], _I),
     "mi_attention": ([_P, _P, _P, _P, _P, _I, _I, _I, _P], _I),
     "mi_gated_add": ([_P, _P, _P, _I, _P, _I, _I, _I, _P], _I),
@@ -271,6 +272,14 @@ def gemm_silu_gate(a, w, m_out, stream=None):
     inter = w.shape[0] // 2
     _check(lib().mi_gemm_bf16_silu_gate(_ptr(a, _BF), _ptr(w, _BF), _ptr(m_out, _BF), m, inter, k,
                                         _stream(stream)))
+
+
+def gemm_qkv_rope(a, w_qkv, q_norm_w, k_norm_w, rope_cos, rope_sin, qp, kp, qkv_v, batch, seq, n_heads, eps=1e-6,
+                  rope_bstride=0, stream=None):
+    _check(lib().mi_gemm_bf16_qkv_rope(_ptr(a, _BF), _ptr(w_qkv, _BF), _ptr(q_norm_w, _BF), _ptr(k_norm_w, _BF),
+                                       _ptr(rope_cos, torch.float32), _ptr(rope_sin, torch.float32), rope_bstride,
+                                       _ptr(qp, _BF), _ptr(kp, _BF), _ptr(qkv_v, _BF), batch, seq, n_heads, eps,
+                                       _stream(stream)))
 
 
 def qk_norm_rope(qkv, q_norm_w, k_norm_w, rope_cos, rope_sin, qp, kp, batch, seq, n_heads, eps=1e-6,

@@ -287,16 +287,31 @@ static mi_status block_forward_impl(mi_block* blk, int batch, int S, const void*
   // 1. modulated RMSNorm #1
   e = mi::mod_rmsnorm_launch(cb(x), md + 0 * H, md + 1 * H, mbs, h, R, S, H, d.eps, s);
   if (e != cudaSuccess) return cuda_fail(e, "mod_rmsnorm");
-  // 2. QKV projection
-  {
+  // 2-3. QKV projection; q/k RMSNorm + rotary, packed per head (fused into the projection's epilogue,
+  // or a separate kernel when epilogues are not fused)
+  if (d.fuse_epilogues) {
+    mi::GemmArgs g = gemm_args(R, 3 * H, H, qkv, dev->err);
+    g.seq = S;
+    g.qp = qp;
+    g.kp = kp;
+    g.wq = cb(d.q_norm_w);
+    g.wk = cb(d.k_norm_w);
+    g.rope_cos = cosv;
+    g.rope_sin = sinv;
+    g.rope_bstride = rope_bstride;
+    g.hidden = H;
+    g.heads = nh;
+    g.eps = d.eps;
+    mi_status st = run_gemm(dev, mi::EPI_QKV_ROPE, tm_h, blk->tm_wqkv, g, s);
+    if (st != MI_OK) return st;
+  } else {
     mi::GemmArgs g = gemm_args(R, 3 * H, H, qkv, dev->err);
     mi_status st = run_gemm(dev, mi::EPI_STORE, tm_h, blk->tm_wqkv, g, s);
     if (st != MI_OK) return st;
+    e = mi::qk_norm_rope_launch(qkv, cb(d.q_norm_w), cb(d.k_norm_w), cosv, sinv, rope_bstride, qp, kp, batch, S, nh,
+                                d.eps, s);
+    if (e != cudaSuccess) return cuda_fail(e, "qk_norm_rope");
   }
-  // 3. q/k RMSNorm + rotary, packed per head
-  e = mi::qk_norm_rope_launch(qkv, cb(d.q_norm_w), cb(d.k_norm_w), cosv, sinv, rope_bstride, qp, kp, batch, S, nh,
-                              d.eps, s);
-  if (e != cudaSuccess) return cuda_fail(e, "qk_norm_rope");
   // 4. attention
   {
     mi::AttnArgs aa;
@@ -683,6 +698,41 @@ mi_status mi_gemm_bf16_gated_residual(const void* a, const void* w, const void* 
 
 mi_status mi_gemm_bf16_silu_gate(const void* a, const void* w, void* m_out, int m, int inter, int k, void* stream) {
   return gemm_common(mi::EPI_SILU_GATE, a, w, m_out, m, inter, k, nullptr, nullptr, 0, 1, stream);
+}
+
+mi_status mi_gemm_bf16_qkv_rope(const void* a, const void* w_qkv, const void* q_norm_w, const void* k_norm_w,
+                                const float* rope_cos, const float* rope_sin, int rope_bstride, void* qp, void* kp,
+                                void* qkv_v, int batch, int seq, int n_heads, float eps, void* stream) {
+  if (!a || !w_qkv || !q_norm_w || !k_norm_w || !rope_cos || !rope_sin || !qp || !kp || !qkv_v)
+    return fail(MI_ERR_INVALID_ARG, "null tensor argument");
+  if (!aligned16(a) || !aligned16(w_qkv) || !aligned16(q_norm_w) || !aligned16(k_norm_w) || !aligned16(rope_cos) ||
+      !aligned16(rope_sin) || !aligned16(qp) || !aligned16(kp) || !aligned16(qkv_v))
+    return fail(MI_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if (batch <= 0 || seq <= 0 || n_heads <= 0) return fail(MI_ERR_INVALID_ARG, "batch, seq, n_heads must be positive");
+  const int H = n_heads * 128;
+  if (H % 256 != 0) return fail(MI_ERR_UNSUPPORTED, "hidden=%d must be a multiple of 256", H);
+  if (rope_bstride < 0 || rope_bstride % 4 != 0) return fail(MI_ERR_INVALID_ARG, "bad rope_bstride");
+  const int m = batch * seq;
+  mi_status st = check_gemm_shape(m, 3 * H, H, mi::EPI_QKV_ROPE);
+  if (st != MI_OK) return st;
+  DeviceInfo* dev = nullptr;
+  st = require_sm103(&dev);
+  if (st != MI_OK) return st;
+  CUtensorMap ta, tb;
+  if (!map_a(&ta, a, m, H) || !map_w(&tb, w_qkv, 3 * H, H, kGemmBN)) return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed");
+  mi::GemmArgs g = gemm_args(m, 3 * H, H, qkv_v, dev->err);
+  g.seq = seq;
+  g.qp = mb(qp);
+  g.kp = mb(kp);
+  g.wq = cb(q_norm_w);
+  g.wk = cb(k_norm_w);
+  g.rope_cos = rope_cos;
+  g.rope_sin = rope_sin;
+  g.rope_bstride = rope_bstride;
+  g.hidden = H;
+  g.heads = n_heads;
+  g.eps = eps;
+  return run_gemm(dev, mi::EPI_QKV_ROPE, ta, tb, g, static_cast<cudaStream_t>(stream));
 }
 
 mi_status mi_qk_norm_rope(const void* qkv, const void* q_norm_w, const void* k_norm_w, const float* rope_cos,

@@ -205,6 +205,67 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+      } else if (EPI == EPI_QKV_ROPE && nb * BN < 2 * p.hidden) {
+        // q or k columns: the tile holds two whole heads of this row.  Per head: round the sums to
+        // bf16 (the QKV projection's rounding point), RMSNorm over the 128 values with the gain,
+        // rotate the pairs (2p, 2p+1) by the row's angles, and write the packed head row.  The
+        // reductions follow the stand-alone q/k kernel's order exactly (sixteen 8-element fma
+        // chains combined by the same butterfly), so fused and unfused results are identical.
+        const int which = nb * BN >= p.hidden ? 1 : 0;
+        const int head0 = (nb * BN - which * p.hidden) / kHeadDim;
+        const __nv_bfloat16* gain = which ? p.wk : p.wq;
+        __nv_bfloat16* dst_base = which ? p.kp : p.qp;
+        const int b = row_ok ? row / p.seq : 0;
+        const int s = row_ok ? row % p.seq : 0;
+#pragma unroll 1
+        for (int hh = 0; hh < BN / kHeadDim; ++hh) {
+          uint32_t r[128];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(t_row + hh * kHeadDim + c * 32, r + c * 32);
+          tmem_ld_wait();
+          if (row_ok) {
+            float part[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              float ss = 0.0f;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float f = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[k * 8 + e])));
+                r[k * 8 + e] = __float_as_uint(f);
+                ss = fmaf(f, f, ss);
+              }
+              part[k] = ss;
+            }
+            float v8[8], w4[4];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v8[k] = part[k] + part[k + 8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w4[k] = v8[k] + v8[k + 4];
+            const float tot = (w4[0] + w4[2]) + (w4[1] + w4[3]);
+            const float rstd = rsqrtf(tot * (1.0f / kHeadDim) + p.eps);
+            const float* cr = p.rope_cos + (size_t)b * p.rope_bstride + (size_t)s * (kHeadDim / 2);
+            const float* sr = p.rope_sin + (size_t)b * p.rope_bstride + (size_t)s * (kHeadDim / 2);
+            uint4* dst = reinterpret_cast<uint4*>(
+                dst_base + (((size_t)b * p.heads + head0 + hh) * p.seq + s) * kHeadDim);
+#pragma unroll
+            for (int v = 0; v < 16; ++v) {  // 8 elements = 4 rotary pairs per 16-byte store
+              const uint4 gv = __ldg(reinterpret_cast<const uint4*>(gain) + v);
+              const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
+              const float4 c4 = __ldg(reinterpret_cast<const float4*>(cr) + v);
+              const float4 s4 = __ldg(reinterpret_cast<const float4*>(sr) + v);
+              const float cs[4] = {c4.x, c4.y, c4.z, c4.w};
+              const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
+              uint32_t w[4];
+#pragma unroll
+              for (int pr = 0; pr < 4; ++pr) {
+                const float a = __uint_as_float(r[v * 8 + 2 * pr]) * rstd * bf16_lo(gs[pr]);
+                const float bb = __uint_as_float(r[v * 8 + 2 * pr + 1]) * rstd * bf16_hi(gs[pr]);
+                w[pr] = pack_bf16x2(fmaf(a, cs[pr], -bb * sn[pr]), fmaf(a, sn[pr], bb * cs[pr]));
+              }
+              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
       } else {
         const int b = row_ok ? row / p.seq : 0;
 #pragma unroll 1
@@ -316,6 +377,8 @@ cudaError_t gemm_launch(int epi, const CUtensorMap& ta, const CUtensorMap& tb, c
       return launch_gemm<256, EPI_SILU_GATE>(ta, tb, a, num_sms, s);
     case EPI_STORE_F32:
       return launch_gemm<256, EPI_STORE_F32>(ta, tb, a, num_sms, s);
+    case EPI_QKV_ROPE:
+      return launch_gemm<256, EPI_QKV_ROPE>(ta, tb, a, num_sms, s);
     default:
       return cudaErrorInvalidValue;
   }

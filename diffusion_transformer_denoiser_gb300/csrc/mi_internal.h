@@ -17,6 +17,8 @@ enum GemmEpilogue : int {
   EPI_GATED_RESIDUAL = 1,  // C = resid + gate[b] * bf16(A W^T)
   EPI_SILU_GATE = 2,       // C[:, j] = silu(bf16(A Wg^T)[:, j]) * bf16(A Wu^T)[:, j], W = [Wg; Wu]
   EPI_STORE_F32 = 3,       // C (fp32) = A W^T, the fp32 sums unrounded (C is a float*, ldc in floats)
+  EPI_QKV_ROPE = 4,        // QKV projection: q/k columns -> per-head RMSNorm + rotary -> qp/kp packed
+                           // [B, heads, S, 128]; v columns -> C (the q/k columns of C are not written)
 };
 
 struct GemmArgs {
@@ -27,8 +29,19 @@ struct GemmArgs {
   int ldr;
   const __nv_bfloat16* gate;   // EPI_GATED_RESIDUAL: gate of batch b at gate + b * gate_bstride
   int gate_bstride;
-  int seq;                     // rows per batch element (selects the gate vector)
+  int seq;                     // rows per batch element (selects the gate vector / rotary row)
   int* err;                    // device error flag
+  // EPI_QKV_ROPE
+  __nv_bfloat16* qp;
+  __nv_bfloat16* kp;
+  const __nv_bfloat16* wq;     // [128] q RMSNorm gain
+  const __nv_bfloat16* wk;     // [128] k RMSNorm gain
+  const float* rope_cos;       // [S, 64] per batch element at b * rope_bstride
+  const float* rope_sin;
+  int rope_bstride;
+  int hidden;                  // H (q columns [0, H), k columns [H, 2H))
+  int heads;
+  float eps;
 };
 
 cudaError_t gemm_launch(int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int num_sms,

@@ -115,7 +115,7 @@ mi_status mi_block_workspace_size(const mi_block* blk, int batch, int seq, size_
 /* Intermediates left in the workspace by the last forward (for parity checks). */
 typedef enum mi_tensor {
   MI_T_H = 0,   /* [B*S, H]  modulated RMSNorm #1 */
-  MI_T_QKV = 1, /* [B*S, 3H] QKV projection */
+  MI_T_QKV = 1, /* [B*S, 3H] QKV projection (with fused epilogues only the v columns [2H, 3H)) */
   MI_T_QP = 2,  /* [B, heads, S, 128] q after norm + rotary */
   MI_T_KP = 3,  /* [B, heads, S, 128] k after norm + rotary */
   MI_T_O = 4,   /* [B*S, H]  attention output, heads concatenated */
@@ -226,6 +226,15 @@ mi_status mi_gemm_bf16_gated_residual(const void* a, const void* w, const void* 
  * (the gate/up projection fused with the SiLU gate).  inter a multiple of 128. */
 mi_status mi_gemm_bf16_silu_gate(const void* a, const void* w, void* m_out, int m, int inter, int k,
                                  void* stream);
+
+/* The QKV projection with the q/k RMSNorm + rotary fused into its epilogue: a [batch * seq, H]
+ * times w_qkv [3H, H]^T; q and k heads go, normalised and rotated, to qp, kp [batch, heads, seq, 128]
+ * (identical bytes to mi_gemm_bf16 followed by mi_qk_norm_rope); the v columns go to columns
+ * [2H, 3H) of qkv_v [batch * seq, 3H] (its q/k columns are not written).  H = heads * 128, a multiple
+ * of 256. */
+mi_status mi_gemm_bf16_qkv_rope(const void* a, const void* w_qkv, const void* q_norm_w, const void* k_norm_w,
+                                const float* rope_cos, const float* rope_sin, int rope_bstride, void* qp, void* kp,
+                                void* qkv_v, int batch, int seq, int n_heads, float eps, void* stream);
 
 /* Per-head RMSNorm (gains q_norm_w / k_norm_w [128]) and rotary of the q and k columns of
  * qkv [batch * seq, 3H], written to qp, kp [batch, heads, seq, 128]. */

@@ -103,6 +103,35 @@ def test_fused_silu_gate_matches_unfused_bytes(m, inter, k):
     assert_parity(to_f64(m2), ref, "gemm+silu gate")
 
 
+@pytest.mark.parametrize("batch,seq,heads", [(1, 74, 2), (2, 210, 4), (1, 4130, 24)])
+def test_fused_qkv_rope_matches_unfused_bytes(batch, seq, heads):
+    mi = require_gpu()
+    H = heads * 128
+    rng = np.random.default_rng(seq + 17 * heads)
+    h = to_dev_bf16(_bits(rng, (batch * seq, H)))
+    w = to_dev_bf16(_bits(rng, (3 * H, H), 0.02))
+    wq = to_dev_bf16(_bits(rng, (128,), 0.02, 1.0))
+    wk = to_dev_bf16(_bits(rng, (128,), 0.02, 1.0))
+    g = mi_synth.Geometry("t", batch, 10, (10,) * batch, 1, seq - 10, H, heads, 256)
+    cos, sin = mi_synth.rope_tables(g)
+    cos, sin = to_dev(cos), to_dev(sin)
+    qkv = torch.empty(batch * seq, 3 * H, dtype=BF, device="cuda")
+    qp1 = torch.empty(batch, heads, seq, 128, dtype=BF, device="cuda")
+    kp1 = torch.empty_like(qp1)
+    mi.gemm(h, w, qkv)
+    mi.qk_norm_rope(qkv, wq, wk, cos, sin, qp1, kp1, batch, seq, heads)
+    qkv2 = torch.zeros_like(qkv)
+    qp2 = torch.empty_like(qp1)
+    kp2 = torch.empty_like(qp1)
+    mi.gemm_qkv_rope(h, w, wq, wk, cos, sin, qp2, kp2, qkv2, batch, seq, heads)
+    torch.cuda.synchronize()
+    assert mi.device_error() == 0
+    assert torch.equal(qp1.view(torch.int16), qp2.view(torch.int16))
+    assert torch.equal(kp1.view(torch.int16), kp2.view(torch.int16))
+    assert torch.equal(qkv[:, 2 * H:].contiguous().view(torch.int16), qkv2[:, 2 * H:].contiguous().view(torch.int16))
+    assert not qkv2[:, :2 * H].any()  # q/k columns are not written
+
+
 # ------------------------------------------------------------------------------ element-wise
 @pytest.mark.parametrize("batch,seq,hidden", [(1, 74, 256), (2, 210, 512), (1, 4130, 3072)])
 def test_mod_rmsnorm_parity(batch, seq, hidden):
