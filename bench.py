@@ -369,6 +369,8 @@ def run_ours(args):
             "clocks": clocks,
             "device_error": err,
         }
+        if not args.no_extras:
+            line["extras"] = extras(mi, torch, devc, stream)
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(g, inp)
         print(json.dumps(line), flush=True)
@@ -377,6 +379,113 @@ def run_ours(args):
 
         dist.destroy_process_group()
     return 0
+
+
+def _gpu_step_params(torch, g, seed, devc):
+    """Seeded weights of a guided step drawn on the GPU with the synthetic recipe's distributions
+    (24 full-size blocks are 5.4 GB; drawing them on the host would dominate the run)."""
+    gen = torch.Generator(device=devc)
+    gen.manual_seed(seed)
+    H, I, C, B = g.hidden, g.mlp_inter, g.latent_ch, g.batch
+    bf = torch.bfloat16
+
+    def rn(*shape, std=1.0, mean=0.0):
+        return (torch.randn(*shape, generator=gen, device=devc) * std + mean).to(bf)
+
+    blocks = [dict(w_qkv=rn(3 * H, H, std=0.02), w_o=rn(H, H, std=0.02), w_gu=rn(2 * I, H, std=0.02),
+                   w_d=rn(H, I, std=0.02), q_norm_w=rn(128, std=0.02, mean=1.0),
+                   k_norm_w=rn(128, std=0.02, mean=1.0)) for _ in range(g.n_blocks)]
+    return dict(blocks=blocks, mods=rn(g.n_blocks, 1, 6, H, std=0.1).expand(g.n_blocks, B, 6, H).contiguous(),
+                w_in=rn(H, C, std=0.02), w_out=rn(C, H, std=0.02),
+                mod_final=rn(1, 2, H, std=0.1).expand(B, 2, H).contiguous(), text=rn(B, g.text_pad, H),
+                latent=torch.randn(g.n_img, C, generator=gen, device=devc).to(bf).float())
+
+
+def extras(mi, torch, devc, stream):
+    """The other workloads, timed with CUDA events: the long-sequence block (34 + 128x128 rows), one
+    guided denoising step at 1024x1024 (24 blocks, batch 2: prompt and padded empty negative) and
+    the 50-step Euler loop of that step (guidance 3, t linear in [1, 0]), replayed from a CUDA graph
+    of one step."""
+    out = {}
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    # long-sequence block
+    g = mi_synth.GEOMETRIES["block_2048"]
+    inp = mi_synth.block_inputs(g, 0)
+
+    def t(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(devc)
+
+    w = inp.weights
+    blk = mi.Block(t(w.w_qkv), t(w.w_o), t(w.w_gu), t(w.w_d), t(w.q_norm_w), t(w.k_norm_w), g.n_heads, g.eps)
+    layout = mi.SeqLayout(g.batch, g.text_pad, g.grid_h, g.grid_w)
+    x = t(inp.x)
+    args = (t(inp.mod), torch.from_numpy(inp.rope_cos).to(devc), torch.from_numpy(inp.rope_sin).to(devc),
+            torch.from_numpy(inp.key_mask).to(devc))
+    ws = torch.empty(blk.workspace_size(g.batch, g.seq), dtype=torch.uint8, device=devc)
+    for _ in range(3):
+        blk.forward(layout, x, x, *args, ws)
+    reps = 20
+    e0.record(stream)
+    for _ in range(reps):
+        blk.forward(layout, x, x, *args, ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    gf, af = flops_of(g)
+    out["block_2048"] = {"ms_per_block": ms, "image_tokens_per_s": g.n_img / (ms * 1e-3),
+                         "tflops": (gf + af) / (ms * 1e-3) / 1e12}
+    del blk, x, ws, args
+    # guided step and 50-step loop
+    g = mi_synth.GEOMETRIES["step_1024_cfg"]
+    prm = _gpu_step_params(torch, g, 7, devc)
+    model = mi.Model(prm["blocks"], prm["w_in"], prm["w_out"], g.n_heads, g.eps)
+    layout = mi.SeqLayout(g.batch, g.text_pad, g.grid_h, g.grid_w)
+    ws = torch.empty(model.workspace_size(layout), dtype=torch.uint8, device=devc)
+    cos, sin = (torch.from_numpy(a).to(devc) for a in mi_synth.rope_tables(g))
+    mask = torch.from_numpy(mi_synth.key_mask(g)).to(devc)
+    lat = prm["latent"].clone()
+    ts = mi_synth.euler_schedule(50)
+    dt = float(ts[1] - ts[0])
+
+    def step():
+        model.denoise_step(layout, lat, prm["text"], prm["mods"], prm["mod_final"], cos, sin, mask, dt, 3.0, ws)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    reps = 10
+    e0.record(stream)
+    for _ in range(reps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    valid = sum(g.n_img + nt for nt in g.n_text)  # rows whose keys are valid, per batch element
+    gemm_f = 2 * g.seq * g.batch * (4 * g.hidden ** 2 + 3 * g.hidden * g.mlp_inter) * g.n_blocks
+    attn_f = sum(4 * g.seq * (g.n_img + nt) * 128 * g.n_heads for nt in g.n_text) * g.n_blocks
+    out["step_1024_cfg"] = {"ms_per_step": ms, "tflops": (gemm_f + attn_f) / (ms * 1e-3) / 1e12,
+                            "blocks": g.n_blocks, "batch": g.batch, "valid_rows": valid}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    lat.copy_(prm["latent"])
+    graph.replay()
+    torch.cuda.synchronize()
+    lat.copy_(prm["latent"])
+    gstream = torch.cuda.current_stream()
+    e0.record(gstream)
+    for _ in range(50):
+        graph.replay()
+    e1.record(gstream)
+    torch.cuda.synchronize()
+    out["loop_1024_cfg50"] = {"seconds": e0.elapsed_time(e1) * 1e-3, "steps": 50, "guidance": 3.0,
+                              "launch": "one CUDA graph of one step, replayed 50 times",
+                              "latent_finite": bool(torch.isfinite(lat).all().item())}
+    err = mi.device_error()
+    if err:
+        out["device_error"] = err
+    return out
 
 
 def kernel_times(mi, torch, g, inp, t, devc, stream, reps):
@@ -465,6 +574,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(mi_synth.GEOMETRIES))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the long-sequence block and guided-step timings")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
