@@ -461,9 +461,10 @@ def extras(mi, torch, devc, stream):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
-    valid = sum(g.n_img + nt for nt in g.n_text)  # rows whose keys are valid, per batch element
-    gemm_f = 2 * g.seq * g.batch * (4 * g.hidden ** 2 + 3 * g.hidden * g.mlp_inter) * g.n_blocks
-    attn_f = sum(4 * g.seq * (g.n_img + nt) * 128 * g.n_heads for nt in g.n_text) * g.n_blocks
+    # algorithmic work counts valid rows only (the padded negative rows run but are not credited)
+    valid = sum(g.n_img + nt for nt in g.n_text)
+    gemm_f = sum(2 * (g.n_img + nt) * (4 * g.hidden ** 2 + 3 * g.hidden * g.mlp_inter) for nt in g.n_text) * g.n_blocks
+    attn_f = sum(4 * (g.n_img + nt) ** 2 * 128 * g.n_heads for nt in g.n_text) * g.n_blocks
     out["step_1024_cfg"] = {"ms_per_step": ms, "tflops": (gemm_f + attn_f) / (ms * 1e-3) / 1e12,
                             "blocks": g.n_blocks, "batch": g.batch, "valid_rows": valid}
     graph = torch.cuda.CUDAGraph()
