@@ -16,7 +16,7 @@ import torch
 __all__ = [
     "MiError", "lib", "library_path", "Block", "Model", "SeqLayout", "mod_rmsnorm", "gemm",
     "gemm_gated_residual", "gemm_silu_gate", "gemm_qkv_rope", "qk_norm_rope", "attention", "gated_add", "silu_gate",
-    "device_error", "device_supported", "TENSORS",
+    "device_error", "device_supported", "TENSORS", "TimestepModulation", "rope_tables", "time_advance",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -53,6 +53,11 @@ class SeqLayout(ctypes.Structure):
         return self.text_pad + self.grid_h * self.grid_w
 
 
+class _TmodDesc(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("n_blocks", ctypes.c_int), ("w_t1", ctypes.c_void_p),
+                ("w_t2", ctypes.c_void_p), ("w_mod", ctypes.c_void_p)]
+
+
 class _ModelDesc(ctypes.Structure):
     _fields_ = [("n_blocks", ctypes.c_int), ("blocks", ctypes.POINTER(_BlockDesc)),
                 ("latent_ch", ctypes.c_int), ("w_in", ctypes.c_void_p), ("w_out", ctypes.c_void_p)]
@@ -80,6 +85,12 @@ _SIGNATURES = {
     "mi_model_workspace_size": ([_P, ctypes.POINTER(SeqLayout), ctypes.POINTER(_SZ)], _I),
     "mi_denoise_step": ([_P, ctypes.POINTER(SeqLayout), _P, _P, _P, _P, _P, _P, _I, _P, _F, _F, _P, _P, _SZ,
                          _P], _I),
+    "mi_rope_tables": ([_I, _I, _I, _F, _P, _P, _P], _I),
+    "mi_tmod_init": ([ctypes.POINTER(_P), ctypes.POINTER(_TmodDesc)], _I),
+    "mi_tmod_destroy": ([_P], None),
+    "mi_tmod_workspace_size": ([_P, _I, ctypes.POINTER(_SZ)], _I),
+    "mi_timestep_modulation": ([_P, _P, _I, _P, _P, _P, _SZ, _P], _I),
+    "mi_time_advance": ([_P, _I, _F, _P], _I),
     "mi_mod_rmsnorm": ([_P, _P, _I, _I, _P, _I, _I, _I, _F, _P], _I),
     "mi_gemm_bf16": ([_P, _P, _P, _I, _I, _I, _P], _I),
     "mi_gemm_bf16_gated_residual": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
@@ -246,6 +257,48 @@ class Model:
                                      _ptr(rope_sin, torch.float32), rope_bstride, _ptr(key_mask, torch.uint8),
                                      dt, guidance, ctypes.cast(sk, _P) if sk is not None else None, _ptr(ws),
                                      ws.numel() * ws.element_size(), _stream(stream)))
+
+
+class TimestepModulation:
+    """Timestep -> per-block modulation on the device (weights owned by the caller's tensors)."""
+
+    def __init__(self, w_t1, w_t2, w_mod, n_blocks: int):
+        self._keep = (w_t1, w_t2, w_mod)
+        self.hidden, self.n_blocks = w_t2.shape[0], n_blocks
+        self.desc = _TmodDesc(w_t2.shape[0], n_blocks, _ptr(w_t1, _BF), _ptr(w_t2, _BF), _ptr(w_mod, _BF))
+        h = _P()
+        _check(lib().mi_tmod_init(ctypes.byref(h), ctypes.byref(self.desc)))
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().mi_tmod_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def workspace_size(self, batch: int) -> int:
+        n = _SZ(0)
+        _check(lib().mi_tmod_workspace_size(self.handle, batch, ctypes.byref(n)))
+        return n.value
+
+    def __call__(self, t, mods, mod_final, ws, stream=None):
+        _check(lib().mi_timestep_modulation(self.handle, _ptr(t, torch.float32), t.numel(), _ptr(mods, _BF),
+                                            _ptr(mod_final, _BF), _ptr(ws), ws.numel() * ws.element_size(),
+                                            _stream(stream)))
+
+
+def rope_tables(text_pad, grid_h, grid_w, rope_cos, rope_sin, theta=10000.0, stream=None):
+    _check(lib().mi_rope_tables(text_pad, grid_h, grid_w, theta, _ptr(rope_cos, torch.float32),
+                                _ptr(rope_sin, torch.float32), _stream(stream)))
+
+
+def time_advance(t, dt, stream=None):
+    _check(lib().mi_time_advance(_ptr(t, torch.float32), t.numel(), dt, _stream(stream)))
 
 
 # ------------------------------------------------------------------------------- single kernels

@@ -857,3 +857,135 @@ extern "C" mi_status mi_block_forward_static_ws(mi_block* blk, const mi_seq_layo
   if (st != MI_OK) return st;
   return mi_block_forward(blk, L, x, y, mod, rope_cos, rope_sin, rope_bstride, key_mask, ws, kStaticWsBytes, stream);
 }
+
+// ------------------------------------------------------------------------------ device builders
+struct mi_tmod {
+  mi_tmod_desc d;
+  CUtensorMap tm_w1, tm_w2, tm_wmod;
+};
+
+namespace {
+
+constexpr int kTDim = 256;
+constexpr double kTScale = 1000.0;
+constexpr double kTMaxPeriod = 10000.0;
+
+struct TmodLayout {
+  size_t emb, a1, c, all, total;
+};
+
+TmodLayout plan_tmod(const mi_tmod_desc& d, int batch) {
+  TmodLayout l;
+  const size_t H = d.hidden, rows_all = (size_t)(6 * d.n_blocks + 2) * H;
+  size_t cur = 0;
+  l.emb = cur;
+  cur = align_up(cur + (size_t)batch * kTDim * 2, 1024);
+  l.a1 = cur;
+  cur = align_up(cur + (size_t)batch * H * 2, 1024);
+  l.c = cur;
+  cur = align_up(cur + (size_t)batch * H * 2, 1024);
+  l.all = cur;
+  cur = align_up(cur + (size_t)batch * rows_all * 2, 1024);
+  l.total = cur;
+  return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+mi_status mi_tmod_init(mi_tmod** out, const mi_tmod_desc* desc) {
+  if (!out || !desc) return fail(MI_ERR_INVALID_ARG, "null argument");
+  *out = nullptr;
+  if (desc->hidden <= 0 || desc->hidden % 256 != 0) return fail(MI_ERR_UNSUPPORTED, "hidden must be a multiple of 256");
+  if (desc->n_blocks <= 0) return fail(MI_ERR_INVALID_ARG, "n_blocks must be positive");
+  if (!desc->w_t1 || !desc->w_t2 || !desc->w_mod || !aligned16(desc->w_t1) || !aligned16(desc->w_t2) ||
+      !aligned16(desc->w_mod))
+    return fail(MI_ERR_INVALID_ARG, "weights must be non-null and 16-byte aligned");
+  DeviceInfo* dev = nullptr;
+  mi_status st = require_sm103(&dev);
+  if (st != MI_OK) return st;
+  mi_tmod* m = new (std::nothrow) mi_tmod;
+  if (!m) return fail(MI_ERR_INVALID_ARG, "host allocation failed");
+  m->d = *desc;
+  const int H = desc->hidden;
+  if (!map_w(&m->tm_w1, desc->w_t1, H, kTDim, kGemmBN) || !map_w(&m->tm_w2, desc->w_t2, H, H, kGemmBN) ||
+      !map_w(&m->tm_wmod, desc->w_mod, (6 * desc->n_blocks + 2) * H, H, kGemmBN)) {
+    delete m;
+    return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed (timestep weights)");
+  }
+  *out = m;
+  return MI_OK;
+}
+
+void mi_tmod_destroy(mi_tmod* tm) { delete tm; }
+
+mi_status mi_tmod_workspace_size(const mi_tmod* tm, int batch, size_t* bytes) {
+  if (!tm || !bytes || batch <= 0) return fail(MI_ERR_INVALID_ARG, "bad argument");
+  *bytes = plan_tmod(tm->d, batch).total;
+  return MI_OK;
+}
+
+mi_status mi_timestep_modulation(mi_tmod* tm, const float* t, int batch, void* mods, void* mod_final, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  if (!tm || !t || !mods || !mod_final) return fail(MI_ERR_INVALID_ARG, "null argument");
+  if (batch <= 0 || batch > 128) return fail(MI_ERR_INVALID_ARG, "batch must be in [1, 128]");
+  if (!aligned16(mods) || !aligned16(mod_final)) return fail(MI_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
+  const TmodLayout l = plan_tmod(tm->d, batch);
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(MI_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
+  if (ws_bytes < l.total) return fail(MI_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, l.total);
+  DeviceInfo* dev = nullptr;
+  mi_status st = require_sm103(&dev);
+  if (st != MI_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int H = tm->d.hidden, nb = tm->d.n_blocks;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  bf16* emb = mb(base + l.emb);
+  bf16* a1 = mb(base + l.a1);
+  bf16* c = mb(base + l.c);
+  bf16* all = mb(base + l.all);
+  cudaError_t e = mi::timestep_embedding_launch(t, emb, batch, kTDim, kTScale, kTMaxPeriod, s);
+  if (e != cudaSuccess) return cuda_fail(e, "timestep embedding");
+  CUtensorMap ta;
+  if (!map_a(&ta, emb, batch, kTDim)) return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed");
+  st = run_gemm(dev, mi::EPI_STORE, ta, tm->tm_w1, gemm_args(batch, H, kTDim, a1, dev->err), s);
+  if (st != MI_OK) return st;
+  e = mi::silu_inplace_launch(a1, (long long)batch * H, s);
+  if (e != cudaSuccess) return cuda_fail(e, "silu");
+  if (!map_a(&ta, a1, batch, H)) return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed");
+  st = run_gemm(dev, mi::EPI_STORE, ta, tm->tm_w2, gemm_args(batch, H, H, c, dev->err), s);
+  if (st != MI_OK) return st;
+  e = mi::silu_inplace_launch(c, (long long)batch * H, s);
+  if (e != cudaSuccess) return cuda_fail(e, "silu");
+  if (!map_a(&ta, c, batch, H)) return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed");
+  st = run_gemm(dev, mi::EPI_STORE, ta, tm->tm_wmod, gemm_args(batch, (6 * nb + 2) * H, H, all, dev->err), s);
+  if (st != MI_OK) return st;
+  e = mi::modulation_split_launch(all, mb(mods), mb(mod_final), batch, nb, H, s);
+  return e == cudaSuccess ? MI_OK : cuda_fail(e, "modulation split");
+}
+
+mi_status mi_rope_tables(int text_pad, int grid_h, int grid_w, float theta, float* rope_cos, float* rope_sin,
+                         void* stream) {
+  if (!rope_cos || !rope_sin) return fail(MI_ERR_INVALID_ARG, "null argument");
+  if (text_pad < 0 || grid_h < 0 || grid_w <= 0 || !(theta > 1.0f)) return fail(MI_ERR_INVALID_ARG, "bad geometry");
+  const long long S = (long long)text_pad + (long long)grid_h * grid_w;
+  if (S <= 0 || S > (1 << 20)) return fail(MI_ERR_INVALID_ARG, "sequence length out of range");
+  DeviceInfo* dev = nullptr;
+  mi_status st = require_sm103(&dev);
+  if (st != MI_OK) return st;
+  cudaError_t e = mi::rope_table_launch(rope_cos, rope_sin, (int)S, text_pad, grid_w, (double)theta,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MI_OK : cuda_fail(e, "rope tables");
+}
+
+mi_status mi_time_advance(float* t, int n, float dt, void* stream) {
+  if (!t || n <= 0) return fail(MI_ERR_INVALID_ARG, "bad argument");
+  DeviceInfo* dev = nullptr;
+  mi_status st = require_sm103(&dev);
+  if (st != MI_OK) return st;
+  cudaError_t e = mi::time_advance_launch(t, n, dt, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MI_OK : cuda_fail(e, "time advance");
+}
+
+}  // extern "C"

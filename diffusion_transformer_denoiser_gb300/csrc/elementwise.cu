@@ -216,6 +216,73 @@ __global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float* __restric
     dst[i] = __float2bfloat16_rn(src[i]);
 }
 
+// ------------------------------------------------------------------------------------ builders
+// Rotary tables on the device: row s, pair j turns by pos * theta^(-(j mod 32)/32) with pos the row
+// position (pairs < 32) or column position (pairs >= 32) of the token; text row t has position t
+// on both axes.  Angles in fp64, stored as fp32.
+__global__ void __launch_bounds__(256) rope_table_kernel(float* __restrict__ cosv, float* __restrict__ sinv, int S,
+                                                          int text_pad, int grid_w, double theta) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= S * 64) return;
+  const int s = i >> 6;
+  const int j = i & 63;
+  double pos;
+  if (s < text_pad) {
+    pos = (double)s;
+  } else {
+    const int r = (s - text_pad) / grid_w;
+    const int c = (s - text_pad) % grid_w;
+    pos = (double)(j < 32 ? r : c);
+  }
+  const double ang = pos * pow(theta, -(double)(j & 31) / 32.0);
+  cosv[i] = (float)cos(ang);
+  sinv[i] = (float)sin(ang);
+}
+
+// Sinusoidal timestep embedding: out[b, k] = cos(scale t_b f_k), out[b, half + k] = sin(scale t_b f_k),
+// f_k = max_period^(-k / half); fp64, rounded to bf16.
+__global__ void __launch_bounds__(256) timestep_embedding_kernel(const float* __restrict__ t, __nv_bfloat16* __restrict__ out,
+                                                                 int batch, int half, double scale, double max_period) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= batch * half) return;
+  const int b = i / half;
+  const int k = i % half;
+  const double ang = scale * (double)t[b] * pow(max_period, -(double)k / (double)half);
+  out[(size_t)b * 2 * half + k] = __float2bfloat16_rn((float)cos(ang));
+  out[(size_t)b * 2 * half + half + k] = __float2bfloat16_rn((float)sin(ang));
+}
+
+__global__ void __launch_bounds__(256) silu_inplace_kernel(__nv_bfloat16* __restrict__ v, long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    v[i] = __float2bfloat16_rn(silu_f(__bfloat162float(v[i])));
+}
+
+// all[b, (6 i + k) H + c] -> mods[i, b, k, c]; all[b, (6 n + k) H + c] -> final[b, k, c].
+__global__ void __launch_bounds__(256) modulation_split_kernel(const uint4* __restrict__ all, uint4* __restrict__ mods,
+                                                               uint4* __restrict__ fin, int batch, int n_blocks,
+                                                               int vpr /* H / 8 */) {
+  const long long per_b = (long long)(6 * n_blocks + 2) * vpr;
+  const long long total = per_b * batch;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int b = (int)(i / per_b);
+    const long long r = i % per_b;
+    const int vec = (int)(r / vpr);  // which H-wide vector
+    const int c = (int)(r % vpr);
+    if (vec < 6 * n_blocks) {
+      const int blk = vec / 6, k = vec % 6;
+      mods[(((long long)blk * batch + b) * 6 + k) * vpr + c] = all[i];
+    } else {
+      fin[((long long)b * 2 + (vec - 6 * n_blocks)) * vpr + c] = all[i];
+    }
+  }
+}
+
+__global__ void time_advance_kernel(float* __restrict__ t, int n, float dt) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) t[i] += dt;
+}
+
 int grid_for(long long work_items, int threads) {
   long long g = (work_items + threads - 1) / threads;
   const long long cap = 152LL * 16;  // enough resident blocks for a grid-stride loop
@@ -298,6 +365,41 @@ cudaError_t cfg_euler_launch(const float* vel, float* latent, int n_img, int cha
   const long long n = (long long)n_img * channels;
   if (n <= 0) return cudaSuccess;
   cfg_euler_kernel<<<grid_for(n, 256), 256, 0, s>>>(vel, latent, n, dt, guidance, batch);
+  return cudaGetLastError();
+}
+
+cudaError_t rope_table_launch(float* cosv, float* sinv, int S, int text_pad, int grid_w, double theta, cudaStream_t s) {
+  if (S <= 0) return cudaSuccess;
+  rope_table_kernel<<<(S * 64 + 255) / 256, 256, 0, s>>>(cosv, sinv, S, text_pad, grid_w, theta);
+  return cudaGetLastError();
+}
+
+cudaError_t timestep_embedding_launch(const float* t, __nv_bfloat16* out, int batch, int dim, double scale,
+                                      double max_period, cudaStream_t s) {
+  const int half = dim / 2;
+  timestep_embedding_kernel<<<(batch * half + 255) / 256, 256, 0, s>>>(t, out, batch, half, scale, max_period);
+  return cudaGetLastError();
+}
+
+cudaError_t silu_inplace_launch(__nv_bfloat16* v, long long n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  silu_inplace_kernel<<<grid_for(n, 256), 256, 0, s>>>(v, n);
+  return cudaGetLastError();
+}
+
+cudaError_t modulation_split_launch(const __nv_bfloat16* all, __nv_bfloat16* mods, __nv_bfloat16* fin, int batch,
+                                    int n_blocks, int hidden, cudaStream_t s) {
+  const long long total = (long long)batch * (6 * n_blocks + 2) * (hidden / 8);
+  modulation_split_kernel<<<grid_for(total, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(all),
+                                                               reinterpret_cast<uint4*>(mods),
+                                                               reinterpret_cast<uint4*>(fin), batch, n_blocks,
+                                                               hidden / 8);
+  return cudaGetLastError();
+}
+
+cudaError_t time_advance_launch(float* t, int n, float dt, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  time_advance_kernel<<<(n + 255) / 256, 256, 0, s>>>(t, n, dt);
   return cudaGetLastError();
 }
 

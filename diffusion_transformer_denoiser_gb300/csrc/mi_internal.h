@@ -78,6 +78,13 @@ cudaError_t copy_rows_launch(const __nv_bfloat16* src, __nv_bfloat16* dst, size_
 cudaError_t cfg_euler_launch(const float* vel, float* latent, int n_img, int channels, float dt, float guidance,
                              int batch, cudaStream_t s);
 cudaError_t f32_to_bf16_launch(const float* src, __nv_bfloat16* dst, size_t n, cudaStream_t s);
+cudaError_t rope_table_launch(float* cosv, float* sinv, int S, int text_pad, int grid_w, double theta, cudaStream_t s);
+cudaError_t timestep_embedding_launch(const float* t, __nv_bfloat16* out, int batch, int dim, double scale,
+                                      double max_period, cudaStream_t s);
+cudaError_t silu_inplace_launch(__nv_bfloat16* v, long long n, cudaStream_t s);
+cudaError_t modulation_split_launch(const __nv_bfloat16* all, __nv_bfloat16* mods, __nv_bfloat16* fin, int batch,
+                                    int n_blocks, int hidden, cudaStream_t s);
+cudaError_t time_advance_launch(float* t, int n, float dt, cudaStream_t s);
 
 // Self-test of the bounded pipeline waits (selftest.cu).
 cudaError_t wait_timeout_selftest_launch(int* err, unsigned long long limit_ns, cudaStream_t s);

@@ -205,6 +205,43 @@ mi_status mi_denoise_step(mi_model* model, const mi_seq_layout* L, void* latent,
                           int rope_bstride, const uint8_t* key_mask, float dt, float guidance,
                           const uint8_t* skip_neg, void* ws, size_t ws_bytes, void* stream);
 
+/* ----------------------------------------------------------------------- device builders --- */
+/* The per-step inputs the pages compute on the host (PR #1528 "What it adds": "the config, rotary
+ * tables and the timestep's modulation are shared"), computed on the device so a whole guided
+ * loop can run without the host. */
+
+/* Rotary tables (fp32 [S, 64], S = text_pad + grid_h * grid_w): pair j < 32 of row s turns by
+ * (row position) * theta^(-j/32), pair j >= 32 by (column position) * theta^(-(j-32)/32); text row
+ * t has position t on both axes, image token (r, c) has (r, c).  Angles in fp64, stored fp32. */
+mi_status mi_rope_tables(int text_pad, int grid_h, int grid_w, float theta, float* rope_cos, float* rope_sin,
+                         void* stream);
+
+typedef struct mi_tmod_desc {
+  int hidden;          /* H, multiple of 256 */
+  int n_blocks;
+  const void* w_t1;    /* bf16 [H, 256] */
+  const void* w_t2;    /* bf16 [H, H] */
+  const void* w_mod;   /* bf16 [(6 n_blocks + 2) H, H]: block i's six vectors (shift1, scale1, gate1,
+                          shift2, scale2, gate2) at rows [6 i H, 6 (i + 1) H), then shift_f, scale_f */
+} mi_tmod_desc;
+
+typedef struct mi_tmod mi_tmod;
+
+mi_status mi_tmod_init(mi_tmod** out, const mi_tmod_desc* desc);
+void mi_tmod_destroy(mi_tmod* tm);
+mi_status mi_tmod_workspace_size(const mi_tmod* tm, int batch, size_t* bytes);
+
+/* Timestep -> modulation of every block and of the final norm, on the device:
+ *   emb = [cos(1000 t f_k), sin(1000 t f_k)], f_k = 10000^(-k/128), k < 128  (256 values)
+ *   c = W_t2 silu(W_t1 emb);  all = W_mod silu(c)
+ * with a bf16 rounding after every step.  t: device fp32 [batch]; mods: bf16 [n_blocks, batch, 6, H]
+ * (the layout mi_denoise_step reads); mod_final: bf16 [batch, 2, H]. */
+mi_status mi_timestep_modulation(mi_tmod* tm, const float* t, int batch, void* mods, void* mod_final, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/* t[i] += dt for i < n (device fp32), so a captured step can advance its own timestep. */
+mi_status mi_time_advance(float* t, int n, float dt, void* stream);
+
 /* ------------------------------------------------------------------------ single kernels --- */
 /* The steps of the block as separate calls (same kernels mi_block_forward launches). */
 

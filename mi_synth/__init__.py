@@ -230,3 +230,20 @@ def step_inputs(g: Geometry, seed: int = 0) -> StepInputs:
 def euler_schedule(n_steps: int) -> np.ndarray:
     """Timesteps t_i = 1 - i/n for i = 0..n (linear in [1, 0]); step i moves by t_{i+1} - t_i."""
     return 1.0 - np.arange(n_steps + 1, dtype=np.float64) / n_steps
+
+
+@dataclass
+class TimestepWeights:
+    """Weights of the timestep -> modulation path: W_t1 [H, 256], W_t2 [H, H] and the stacked
+    projection W_mod [(6 n_blocks + 2) H, H], all ~ N(0, 0.02) (bf16 bits)."""
+
+    w_t1: np.ndarray
+    w_t2: np.ndarray
+    w_mod: np.ndarray
+
+
+def timestep_weights(g: Geometry, seed: int = 0) -> TimestepWeights:
+    rng = np.random.default_rng(seed)
+    H = g.hidden
+    return TimestepWeights(bf16_bits(_normal(rng, (H, 256), 0.02)), bf16_bits(_normal(rng, (H, H), 0.02)),
+                           bf16_bits(_normal(rng, ((6 * g.n_blocks + 2) * H, H), 0.02)))

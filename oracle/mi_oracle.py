@@ -346,6 +346,54 @@ def step_inputs_widened(si):
                 key_mask=si.key_mask, n_heads=si.geom.n_heads)
 
 
+# ----------------------------------------------------------------------------------------------
+# device-side builders (PR #1528 "What it adds": the config, rotary tables and the timestep's
+# modulation are computed by host code shared with the Metal family; here they are computed on
+# the device, and these are their definitions)
+# ----------------------------------------------------------------------------------------------
+def rope_angle_tables(text_pad, grid_h, grid_w, theta=10000.0):
+    """cos/sin [S, 64] of the 2-D rotary: pair j < 32 turns by (row position) * theta^(-j/32), pair
+    j >= 32 by (column position) * theta^(-(j-32)/32); text row t has position t on both axes,
+    image token (r, c) (row-major after the text) has (r, c)."""
+    S = text_pad + grid_h * grid_w
+    cos = np.empty((S, 64))
+    sin = np.empty((S, 64))
+    for s in range(S):
+        if s < text_pad:
+            pa = pb = float(s)
+        else:
+            pa, pb = divmod(s - text_pad, grid_w)
+        for j in range(64):
+            pos = pa if j < 32 else pb
+            ang = pos * theta ** (-(j % 32) / 32.0)
+            cos[s, j] = np.cos(ang)
+            sin[s, j] = np.sin(ang)
+    return cos, sin
+
+
+def timestep_embedding(t, dim=256, scale=1000.0, max_period=10000.0):
+    """Sinusoidal embedding of scale * t: [cos(scale t f_k) for k < dim/2, sin(scale t f_k) for
+    k < dim/2] with f_k = max_period^(-k / (dim/2)).  t: [B] -> [B, dim]."""
+    t = np.asarray(t, dtype=np.float64)
+    half = dim // 2
+    f = max_period ** (-np.arange(half, dtype=np.float64) / half)
+    ang = scale * t[:, None] * f[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1)
+
+
+def timestep_modulation(t, w_t1, w_t2, w_mod, n_blocks):
+    """Modulation of every block and of the final norm from the timestep:
+    c = W_t2 silu(W_t1 emb(t)); all = W_mod silu(c) with W_mod [(6 n_blocks + 2) H, H].
+    Returns (mods [n_blocks, B, 6, H], mod_final [B, 2, H])."""
+    H = w_t2.shape[0]
+    c = project(silu(project(timestep_embedding(t, w_t1.shape[1]), w_t1)), w_t2)
+    allv = project(silu(c), w_mod)
+    B = allv.shape[0]
+    mods = allv[:, : 6 * n_blocks * H].reshape(B, n_blocks, 6, H).transpose(1, 0, 2, 3)
+    final = allv[:, 6 * n_blocks * H:].reshape(B, 2, H)
+    return mods, final
+
+
 def euler_loop(latent, timesteps, step_fn):
     """Run step_fn(latent, dt) over the schedule's consecutive differences dt_i = t_{i+1} - t_i."""
     x = latent

@@ -541,3 +541,59 @@ def test_row_subset_forward_matches_full_forward():
                                inp.rope_cos.astype(np.float64), inp.rope_sin.astype(np.float64), rows,
                                inp.key_mask, g.n_heads)
     np.testing.assert_allclose(sub, full[rows], rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------ device-side builders
+def test_rope_angle_tables_pins():
+    cos, sin = O.rope_angle_tables(3, 4, 5)
+    np.testing.assert_allclose(cos ** 2 + sin ** 2, 1.0, atol=1e-15)
+    # pair 0 has frequency 1: the angle is the position itself
+    assert abs(cos[2, 0] - math.cos(2.0)) < 1e-15 and abs(sin[2, 32] - math.sin(2.0)) < 1e-15
+    # image token (r, c) = (1, 3): row axis on the first half, column axis on the second
+    s = 3 + 1 * 5 + 3
+    w = 10000.0 ** (-5 / 32)
+    assert abs(cos[s, 5] - math.cos(1 * w)) < 1e-15 and abs(cos[s, 37] - math.cos(3 * w)) < 1e-15
+    # text row t and image token (t, t) share every angle
+    t = 2
+    assert np.array_equal(cos[t], cos[3 + t * 5 + t]) and np.array_equal(sin[t], sin[3 + t * 5 + t])
+    # consecutive columns differ by one rotation step: angle addition on the column half
+    a = 3 + 2 * 5
+    j = 40
+    w = 10000.0 ** (-(j - 32) / 32)
+    rot = cos[a, j] * math.cos(w) - sin[a, j] * math.sin(w)
+    assert abs(rot - cos[a + 1, j]) < 1e-14
+
+
+def test_rope_angle_tables_match_the_input_tables():
+    g = mi_synth.GEOMETRIES["small_ragged_17x19"]
+    cos, sin = O.rope_angle_tables(g.text_pad, g.grid_h, g.grid_w)
+    c32, s32 = mi_synth.rope_tables(g)
+    assert np.array_equal(cos.astype(np.float32), c32) and np.array_equal(sin.astype(np.float32), s32)
+
+
+def test_timestep_embedding_pins():
+    e0 = O.timestep_embedding([0.0])
+    assert np.all(e0[0, :128] == 1.0) and np.all(e0[0, 128:] == 0.0)
+    e = O.timestep_embedding([0.37, 0.8])
+    np.testing.assert_allclose((e ** 2).sum(axis=1), 128.0, rtol=1e-13)
+    assert abs(e[0, 0] - math.cos(370.0)) < 1e-12 and abs(e[1, 128] - math.sin(800.0)) < 1e-12
+    assert abs(e[0, 127] - math.cos(370.0 * 10000.0 ** (-127 / 128))) < 1e-12
+
+
+def test_timestep_modulation_pins():
+    rng = _rng(21)
+    H, n = 256, 3
+    w1 = rng.standard_normal((H, 256)) * 0.05
+    w2 = rng.standard_normal((H, H)) * 0.05
+    wm = rng.standard_normal(((6 * n + 2) * H, H)) * 0.05
+    mods, fin = O.timestep_modulation([0.25, 0.25], w1, w2, wm, n)
+    assert mods.shape == (n, 2, 6, H) and fin.shape == (2, 2, H)
+    assert np.array_equal(mods[:, 0], mods[:, 1])  # the same timestep gives the same vectors
+    # block i's k-th vector is rows [(6 i + k) H, (6 i + k + 1) H) of W_mod applied to silu(c)
+    c = O.silu(w1 @ O.timestep_embedding([0.25])[0]) @ w2.T
+    sc = O.silu(c)
+    np.testing.assert_allclose(mods[1, 0, 4], wm[(6 + 4) * H:(6 + 5) * H] @ sc, atol=1e-13)
+    np.testing.assert_allclose(fin[0, 1], wm[(6 * n + 1) * H:(6 * n + 2) * H] @ sc, atol=1e-13)
+    # zero projection gives zero modulation
+    m0, f0 = O.timestep_modulation([0.5], w1, w2, np.zeros_like(wm), n)
+    assert not m0.any() and not f0.any()
