@@ -8,7 +8,7 @@
 //                ring (K and V with their own barriers so a K slot frees as soon as both score
 //                products have read it).  K comes from the packed [B, heads, S, 128] rows; V is
 //                read in place from the QKV projection output through a strided 4-D map.
-//   * warp 1   : one thread issues, per key tile j, in this order
+//   * warp 1   : issues (convergent warp, one elected lane per instruction), per key tile j, in this order
 //                  O0 += P0 V_j,  S0 = Q0 K_{j+1}^T,  O1 += P1 V_j,  S1 = Q1 K_{j+1}^T
 //                so the tensor core works on one query tile while the softmax works on the other.
 //   * warps 2-5 (query tile 0) and 6-9 (query tile 1): one thread per query row.  Scores come
@@ -141,85 +141,87 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(&v_full[j & 1], (j >> 1) & 1, p.err, DEV_TIMEOUT_ATTN + 2);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
-      const uint32_t q_addr = smem_u32(sQ);
-      auto issue_s = [&](int i, int j) {  // S_i = Q_i K_j^T
-        const uint32_t qa = q_addr + (uint32_t)i * TILE_BYTES;
-        const uint32_t ka = smem_u32(sK + (j & 1) * TILE_BYTES);
-        const uint32_t d = tmem_base + TM_S + (uint32_t)i * 128u;
+    // ------------------------------------------------------------------ MMA issuer
+    // The whole warp runs this role convergently; each MMA and commit is issued by one elected lane.
+    constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
+    const uint32_t q_addr = smem_u32(sQ);
+    auto issue_s = [&](int i, int j) {  // S_i = Q_i K_j^T
+      const uint32_t qa = q_addr + (uint32_t)i * TILE_BYTES;
+      const uint32_t ka = smem_u32(sK + (j & 1) * TILE_BYTES);
+      const uint32_t d = tmem_base + TM_S + (uint32_t)i * 128u;
+      const uint64_t qd = sdesc_sw128(qa, 16, 1024);
+      const uint64_t kd = sdesc_sw128(ka, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u;
-          tc_mma_ss(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-        }
-      };
-      auto issue_pv = [&](int i, int j) {  // O_i += P_i V_j, P_i from TMEM
-        const uint32_t va = smem_u32(sV + (j & 1) * TILE_BYTES);
-        const uint32_t pa = tmem_base + TM_S + (uint32_t)i * 128u;
-        const uint32_t d = tmem_base + TM_O + (uint32_t)i * 128u;
+      for (int kk = 0; kk < 8; ++kk) {
+        // the start-address field of a descriptor is in 16-byte units
+        const uint32_t off = ((uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u) >> 4;
+        tc_mma_ss_warp(d, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto issue_pv = [&](int i, int j) {  // O_i += P_i V_j, P_i from TMEM
+      const uint32_t pa = tmem_base + TM_S + (uint32_t)i * 128u;
+      const uint32_t d = tmem_base + TM_O + (uint32_t)i * 128u;
+      const uint64_t vd = sdesc_sw128(smem_u32(sV + (j & 1) * TILE_BYTES), HALF_BYTES, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // 16 keys per step: 8 packed P columns; V is MN-major (two 8-key groups 1024 B apart,
-          // d halves 16 KB apart)
-          tc_mma_ts(d, pa + (uint32_t)kk * 8u, sdesc_sw128(va + (uint32_t)kk * 2048u, HALF_BYTES, 1024), idesc_pv,
-                    (j > 0 || kk > 0) ? 1u : 0u);
-        }
-      };
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.err, DEV_TIMEOUT_ATTN + 3) &&
-                mbar_wait(&k_full[0], 0, abort_flag, p.err, DEV_TIMEOUT_ATTN + 3);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        tc_commit(&s_full[0]);
-        issue_s(1, 0);
-        tc_commit(&s_full[1]);
-        tc_commit(&k_empty[0]);
+      for (int kk = 0; kk < 8; ++kk) {
+        // 16 keys per step: 8 packed P columns; V is MN-major (two 8-key groups 1024 B apart,
+        // d halves 16 KB apart)
+        tc_mma_ts_warp(d, pa + (uint32_t)kk * 8u, vd + (uint32_t)kk * (2048u >> 4), idesc_pv,
+                       (j > 0 || kk > 0) ? 1u : 0u);
       }
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (uint32_t)((j >> 1) & 1);
-        const bool more = j + 1 < n_kv;
-        const int nst = (j + 1) & 1;
-        const uint32_t nph = (uint32_t)(((j + 1) >> 1) & 1);
-        // query tile 0
-        if (!mbar_wait(&p_full[0], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4) ||
-            !mbar_wait(&v_full[st], ph, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_pv(0, j);
-        tc_commit(&o_done[0]);
-        if (more) {
-          if (!mbar_wait(&k_full[nst], nph, abort_flag, p.err, DEV_TIMEOUT_ATTN + 5)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_s(0, j + 1);
-          tc_commit(&s_full[0]);
-        }
-        // query tile 1
-        if (!mbar_wait(&p_full[1], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 6)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_pv(1, j);
-        tc_commit(&o_done[1]);
-        tc_commit(&v_empty[st]);
-        if (more) {
-          issue_s(1, j + 1);
-          tc_commit(&s_full[1]);
-          tc_commit(&k_empty[nst]);
-        }
-      }
-      tc_commit(drain);
-      mbar_wait_drain(drain, 0, p.err, DEV_TIMEOUT_ATTN + 7);
+    };
+    bool ok = mbar_wait_warp(q_full, 0, abort_flag, p.err, DEV_TIMEOUT_ATTN + 3) &&
+              mbar_wait_warp(&k_full[0], 0, abort_flag, p.err, DEV_TIMEOUT_ATTN + 3);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0, 0);
+      tc_commit_warp(&s_full[0]);
+      issue_s(1, 0);
+      tc_commit_warp(&s_full[1]);
+      tc_commit_warp(&k_empty[0]);
     }
+    for (int j = 0; j < n_kv && ok; ++j) {
+      const int st = j & 1;
+      const uint32_t ph = (uint32_t)((j >> 1) & 1);
+      const bool more = j + 1 < n_kv;
+      const int nst = (j + 1) & 1;
+      const uint32_t nph = (uint32_t)(((j + 1) >> 1) & 1);
+      // query tile 0
+      if (!mbar_wait_warp(&p_full[0], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4) ||
+          !mbar_wait_warp(&v_full[st], ph, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      issue_pv(0, j);
+      tc_commit_warp(&o_done[0]);
+      if (more) {
+        if (!mbar_wait_warp(&k_full[nst], nph, abort_flag, p.err, DEV_TIMEOUT_ATTN + 5)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_s(0, j + 1);
+        tc_commit_warp(&s_full[0]);
+      }
+      // query tile 1
+      if (!mbar_wait_warp(&p_full[1], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 6)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      issue_pv(1, j);
+      tc_commit_warp(&o_done[1]);
+      tc_commit_warp(&v_empty[st]);
+      if (more) {
+        issue_s(1, j + 1);
+        tc_commit_warp(&s_full[1]);
+        tc_commit_warp(&k_empty[nst]);
+      }
+    }
+    tc_commit_warp(drain);
+    mbar_wait_drain(drain, 0, p.err, DEV_TIMEOUT_ATTN + 7);
   } else {
     // ------------------------------------------------------------------ softmax / epilogue
     const int wg = (warp - 2) >> 2;  // query tile of this warpgroup

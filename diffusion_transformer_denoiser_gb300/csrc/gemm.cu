@@ -3,7 +3,8 @@
 // The pages' projections are library bf16 GEMMs with fp32 sums (MOSS-Image transformer on CUDA,
 // "What it adds").  Here they run on the 5th-generation tensor cores:
 //   * warp 0   : TMA producer, 128-byte-swizzled A and W tiles into a 4-stage shared-memory ring;
-//   * warp 1   : one elected thread issues tcgen05.mma (M=128, N=BN, K=16) into TMEM;
+//   * warp 1   : issues tcgen05.mma (M=128, N=BN, K=16) into TMEM, the warp convergent and one
+//                elected lane per instruction;
 //   * warps 2-5: epilogue, TMEM -> registers -> bf16 -> global, with the fused element-wise
 //                tails (gated residual add, SiLU gate) applied before the single store.
 // Persistent grid (one CTA per SM), tiles walked M-fastest so the A panel stays in L2, and two
@@ -121,48 +122,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = idesc_bf16(BM, BN, false, false);
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, DEV_TIMEOUT_GEMM + 3)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.err, DEV_TIMEOUT_GEMM + 4)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + stage * L::A_BYTES);
-          const uint32_t b0 = smem_u32(sB + stage * L::B_BYTES);
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(b0 + k * 32, 16, 1024);
-            tc_mma_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-          }
-          tc_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+    // ------------------------------------------------------------------ MMA issuer
+    // The whole warp runs this role convergently; each MMA and commit is issued by one elected lane.
+    constexpr uint32_t idesc = idesc_bf16(BM, BN, false, false);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      if (!mbar_wait_warp(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, DEV_TIMEOUT_GEMM + 3)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait_warp(&full[stage], phase, abort_flag, p.err, DEV_TIMEOUT_GEMM + 4)) {
+          ok = false;
+          break;
         }
-        tc_commit(&tfull[acc]);
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1u;
+        tc_fence_after();
+        const uint64_t ad = sdesc_sw128(smem_u32(sA + stage * L::A_BYTES), 16, 1024);
+        const uint64_t bd = sdesc_sw128(smem_u32(sB + stage * L::B_BYTES), 16, 1024);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          // K slice k starts 32 bytes further along the swizzled row (descriptor units: 16 bytes)
+          tc_mma_ss_warp(d_tmem, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+        }
+        tc_commit_warp(&empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      // drain: all MMAs issued by this thread complete before TMEM is released
-      tc_commit(drain);
-      mbar_wait_drain(drain, 0, p.err, DEV_TIMEOUT_GEMM + 6);
+      tc_commit_warp(&tfull[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
+    // drain: all MMAs issued by this warp complete before TMEM is released
+    tc_commit_warp(drain);
+    mbar_wait_drain(drain, 0, p.err, DEV_TIMEOUT_GEMM + 6);
   } else {
     // ------------------------------------------------------------------ epilogue warps
     const int q = warp & 3;  // TMEM lane quarter this warp may access
