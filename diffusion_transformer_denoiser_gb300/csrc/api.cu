@@ -187,16 +187,18 @@ struct mi_block {
   mi_block_desc d;
   CUtensorMap tm_wqkv, tm_wo, tm_wgu, tm_wgu_split, tm_wd;
   int dev;
+  int num_sms;
 };
 
 struct WsLayout {
   size_t off[11];
   size_t bytes[11];
   bool present[11];
+  size_t sk_off, sk_bytes;  // stream-K scratch of the out and down projections (0 bytes: not used)
   size_t total;
 };
 
-static WsLayout plan_ws(const mi_block_desc& d, int batch, int seq) {
+static WsLayout plan_ws(const mi_block_desc& d, int batch, int seq, int num_sms) {
   WsLayout w;
   const size_t R = (size_t)batch * seq;
   const size_t H = d.hidden, I = d.mlp_inter;
@@ -210,6 +212,13 @@ static WsLayout plan_ws(const mi_block_desc& d, int batch, int seq) {
     w.off[i] = cur;
     if (pres) cur = align_up(cur + w.bytes[i], 1024);
   }
+  // the out (K = H) and down (K = I) projections run one after the other and share the scratch
+  const int Ri = batch * seq;
+  const size_t sk_o = mi::gemm_sk_scratch_bytes(mi::EPI_GATED_RESIDUAL, Ri, (int)H, (int)H, num_sms);
+  const size_t sk_d = mi::gemm_sk_scratch_bytes(mi::EPI_GATED_RESIDUAL, Ri, (int)H, (int)I, num_sms);
+  w.sk_bytes = sk_o > sk_d ? sk_o : sk_d;
+  w.sk_off = cur;
+  cur = align_up(cur + w.sk_bytes, 1024);
   w.total = cur;
   return w;
 }
@@ -250,7 +259,7 @@ static mi_status block_forward_impl(mi_block* blk, int batch, int S, const void*
   const mi_block_desc& d = blk->d;
   const int H = d.hidden, I = d.mlp_inter, nh = d.n_heads;
   const int R = batch * S;
-  const WsLayout w = plan_ws(d, batch, S);
+  const WsLayout w = plan_ws(d, batch, S, blk->num_sms);
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
     return fail(MI_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
   if (ws_bytes < w.total) return fail(MI_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, w.total);
@@ -266,6 +275,7 @@ static mi_status block_forward_impl(mi_block* blk, int batch, int S, const void*
   bf16* gu = mb(base + w.off[MI_T_GU]);
   bf16* m = mb(base + w.off[MI_T_M]);
   bf16* dn = mb(base + w.off[MI_T_DN]);
+  void* sk = w.sk_bytes ? static_cast<void*>(base + w.sk_off) : nullptr;
   const bf16* md = cb(mod);
   const int mbs = 6 * H;  // batch stride of the modulation rows
   cudaError_t e;
@@ -328,6 +338,7 @@ static mi_status block_forward_impl(mi_block* blk, int batch, int S, const void*
   // 5. out projection + gated residual
   if (d.fuse_epilogues) {
     mi::GemmArgs g = gemm_args(R, H, H, x1, dev->err);
+    g.sk_scratch = sk;
     g.resid = cb(x);
     g.ldr = H;
     g.gate = md + 2 * H;
@@ -337,6 +348,7 @@ static mi_status block_forward_impl(mi_block* blk, int batch, int S, const void*
     if (st != MI_OK) return st;
   } else {
     mi::GemmArgs g = gemm_args(R, H, H, a, dev->err);
+    g.sk_scratch = sk;
     mi_status st = run_gemm(dev, mi::EPI_STORE, tm_o, blk->tm_wo, g, s);
     if (st != MI_OK) return st;
     e = mi::gated_add_launch(cb(x), a, md + 2 * H, mbs, x1, R, S, H, s);
@@ -360,6 +372,7 @@ static mi_status block_forward_impl(mi_block* blk, int batch, int S, const void*
   // 8. down projection + gated residual
   if (d.fuse_epilogues) {
     mi::GemmArgs g = gemm_args(R, H, I, y, dev->err);
+    g.sk_scratch = sk;
     g.resid = x1;
     g.ldr = H;
     g.gate = md + 5 * H;
@@ -369,6 +382,7 @@ static mi_status block_forward_impl(mi_block* blk, int batch, int S, const void*
     if (st != MI_OK) return st;
   } else {
     mi::GemmArgs g = gemm_args(R, H, I, dn, dev->err);
+    g.sk_scratch = sk;
     mi_status st = run_gemm(dev, mi::EPI_STORE, tm_m, blk->tm_wd, g, s);
     if (st != MI_OK) return st;
     e = mi::gated_add_launch(x1, dn, md + 5 * H, mbs, mb(y), R, S, H, s);
@@ -423,6 +437,7 @@ mi_status mi_block_init(mi_block** out, const mi_block_desc* desc) {
   mi_block* b = new (std::nothrow) mi_block;
   if (!b) return fail(MI_ERR_INVALID_ARG, "host allocation failed");
   b->d = *desc;
+  b->num_sms = dev->num_sms;
   MI_CUDA(cudaGetDevice(&b->dev), "cudaGetDevice");
   const int H = desc->hidden, I = desc->mlp_inter;
   if (!map_w(&b->tm_wqkv, desc->w_qkv, 3 * H, H, kGemmBN) || !map_w(&b->tm_wo, desc->w_o, H, H, kGemmBN) ||
@@ -440,14 +455,14 @@ void mi_block_destroy(mi_block* blk) { delete blk; }
 mi_status mi_block_workspace_size(const mi_block* blk, int batch, int seq, size_t* bytes) {
   if (!blk || !bytes) return fail(MI_ERR_INVALID_ARG, "null argument");
   if (batch <= 0 || seq <= 0) return fail(MI_ERR_INVALID_ARG, "batch and seq must be positive");
-  *bytes = plan_ws(blk->d, batch, seq).total;
+  *bytes = plan_ws(blk->d, batch, seq, blk->num_sms).total;
   return MI_OK;
 }
 
 mi_status mi_block_tensor_offset(const mi_block* blk, int batch, int seq, int which, size_t* offset, size_t* bytes) {
   if (!blk || !offset || !bytes) return fail(MI_ERR_INVALID_ARG, "null argument");
   if (which < 0 || which > MI_T_DN) return fail(MI_ERR_INVALID_ARG, "unknown tensor %d", which);
-  const WsLayout w = plan_ws(blk->d, batch, seq);
+  const WsLayout w = plan_ws(blk->d, batch, seq, blk->num_sms);
   if (!w.present[which]) return fail(MI_ERR_UNSUPPORTED, "tensor %d is not materialised with fused epilogues", which);
   *offset = w.off[which];
   *bytes = w.bytes[which];
@@ -506,7 +521,7 @@ static StepLayout plan_step(const mi_model* m, int batch, int S, int n_img) {
   l.vel = cur;
   cur = align_up(cur + (size_t)batch * n_img * C * 4, 1024);
   l.blk = cur;
-  cur += plan_ws(m->blocks[0]->d, batch, S).total;
+  cur += plan_ws(m->blocks[0]->d, batch, S, m->blocks[0]->num_sms).total;
   l.total = align_up(cur, 1024);
   return l;
 }
@@ -848,7 +863,7 @@ extern "C" mi_status mi_block_forward_static_ws(mi_block* blk, const mi_seq_layo
   int S = 0;
   mi_status st = check_layout(L, &S);
   if (st != MI_OK) return st;
-  const size_t need = plan_ws(blk->d, L->batch, S).total;
+  const size_t need = plan_ws(blk->d, L->batch, S, blk->num_sms).total;
   if (need > kStaticWsBytes)
     return fail(MI_ERR_WORKSPACE, "this geometry needs a %zu-byte workspace; the static one holds %zu bytes", need,
                 kStaticWsBytes);

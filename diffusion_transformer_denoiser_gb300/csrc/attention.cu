@@ -315,13 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_run = l_run * alpha + sum;
 
       if (j > 0) {
-        // the previous P V product is complete (S_i(j) was issued after it); keep the phases of
-        // o_done in step with the loop
-        if (!mbar_wait_warp(&o_done[wg], (j - 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 9)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        // O_i holds the P V products up to key tile j-1, all complete: S_i(j), whose completion
+        // this warp waited for, was issued after P_i(j-1) V_{j-1} by the same thread, and the
+        // tcgen05 operations of one thread complete in issue order
         if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {

@@ -10,6 +10,15 @@
 // Persistent grid (one CTA per SM), tiles walked M-fastest so the A panel stays in L2, and two
 // TMEM accumulators so the epilogue of tile i overlaps the main loop of tile i+1.  Fixed tile
 // order and fixed K order make every launch bit-identical to the previous one.
+//
+// Stream-K tail: when the tile count is not a multiple of the grid, the last partial wave would
+// leave SMs idle.  Instead, the last full wave and the remainder ("tail tiles", or all tiles when
+// there are fewer tiles than SMs) have their k-blocks spread evenly over the CTAs, each CTA taking
+// its share first.  A share is at least half a tile's k-loop, so a tail tile is split between at
+// most three CTAs.  A CTA holding part of a tail tile writes its fp32 partial sums to scratch and
+// counts its k-blocks into the tile's arrival counter; the CTA whose count completes the tile adds
+// the other parts to its own (still in TMEM) in CTA order, a fixed order, so results still repeat
+// bit for bit, and runs the epilogue.  Nobody waits for another CTA: no co-residency is assumed.
 #include "mi_internal.h"
 #include "ptx.cuh"
 
@@ -32,6 +41,132 @@ struct GemmSmem {
 };
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+// Epilogues that support the stream-K tail (their output is a function of each fp32 sum alone).
+template <int EPI>
+constexpr bool kStreamK = EPI == EPI_STORE || EPI == EPI_GATED_RESIDUAL || EPI == EPI_STORE_F32;
+
+// One unit of work of a CTA: k-blocks [kb0, kb1) of a tile.  slot >= 0 marks a part of a tail
+// tile (its partial-sum slot in scratch); tail is the tile's index among the tail tiles.
+struct Work {
+  int tile, kb0, kb1, slot, tail;
+};
+
+// The schedule shared by the producer, MMA and epilogue warps.  Items 0-2 are the tail tiles this
+// CTA's share of tail k-blocks touches (a share spans less than two tiles' k-loops, so at most
+// three tiles; any may be empty, and a tile the share covers whole is an ordinary item); items from
+// 3 on are its whole tiles, strided by the grid.  get() returns 1 for a valid item, 0 for an empty
+// one and -1 past the end.
+struct Schedule {
+  int kblocks, dp_tiles;     // tiles [0, dp_tiles) whole; [dp_tiles, dp_tiles + tail tiles) stream-K
+  long long u_begin, u_end;  // this CTA's share of the tail's k-block units
+
+  __device__ Schedule(int num_tiles, int kblocks_, int sk_tiles) : kblocks(kblocks_), dp_tiles(num_tiles - sk_tiles) {
+    const long long U = (long long)sk_tiles * kblocks_;
+    u_begin = U * blockIdx.x / gridDim.x;
+    u_end = U * (blockIdx.x + 1) / gridDim.x;
+  }
+
+  __device__ int get(int idx, Work& w) const {
+    if (idx < 3) {
+      const long long t0 = u_begin / kblocks;
+      const long long t = t0 + idx;
+      const long long lo = u_begin > t * kblocks ? u_begin : t * kblocks;
+      const long long hi = u_end < (t + 1) * kblocks ? u_end : (t + 1) * kblocks;
+      if (lo >= hi) return 0;
+      w.tile = dp_tiles + (int)t;
+      w.kb0 = (int)(lo - t * kblocks);
+      w.kb1 = (int)(hi - t * kblocks);
+      w.slot = (w.kb0 == 0 && w.kb1 == kblocks) ? -1 : 2 * (int)blockIdx.x + (t == t0 ? 0 : 1);
+      w.tail = (int)t;
+      return 1;
+    }
+    const int tile = (int)blockIdx.x + (idx - 3) * (int)gridDim.x;
+    if (tile >= dp_tiles) return -1;
+    w.tile = tile;
+    w.kb0 = 0;
+    w.kb1 = kblocks;
+    w.slot = -1;
+    w.tail = -1;
+    return 1;
+  }
+};
+
+// The CTA whose share of tail units holds unit x (the inverse of u_begin = U * b / grid).
+__device__ __forceinline__ int sk_owner(long long x, long long U, int grid) {
+  return (int)(((x + 1) * grid - 1) / U);
+}
+
+// Inputs of the epilogue of 32 consecutive columns of one row: the residual and gate vectors of
+// the gated residual add (nothing for the other stream-K capable epilogues).  All are loaded
+// before any store of the chunk: stores to C could alias the residual, so loads placed after them
+// would each wait for a round trip of their own.
+struct ChunkIn {
+  uint4 x[4], g[4];
+};
+
+template <int EPI>
+__device__ __forceinline__ void load_chunk_in(const GemmArgs& p, int row, int b, int col0, ChunkIn& in) {
+  if (EPI == EPI_GATED_RESIDUAL && col0 < p.N) {
+    const uint4* xr = reinterpret_cast<const uint4*>(p.resid + (size_t)row * p.ldr + col0);
+    const uint4* gr = reinterpret_cast<const uint4*>(p.gate + (size_t)b * p.gate_bstride + col0);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      if (col0 + v * 8 < p.N) {
+        in.x[v] = xr[v];
+        in.g[v] = __ldg(gr + v);
+      }
+    }
+  }
+}
+
+// Epilogue of 32 consecutive fp32 sums (bit patterns in r) of one row for the stream-K capable
+// epilogues: plain store, fp32 store, or x + gate[b] * bf16(sum) with x and gate from `in`.
+template <int EPI>
+__device__ __forceinline__ void store_chunk(const GemmArgs& p, const uint32_t (&r)[32], int row, int col0,
+                                            const ChunkIn& in) {
+  if (EPI == EPI_STORE_F32) {
+    if (col0 < p.N) {
+      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.C) + (size_t)row * p.ldc + col0);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        if (col0 + v * 4 < p.N)
+          dst[v] = make_float4(__uint_as_float(r[v * 4 + 0]), __uint_as_float(r[v * 4 + 1]),
+                               __uint_as_float(r[v * 4 + 2]), __uint_as_float(r[v * 4 + 3]));
+      }
+    }
+  } else if (col0 < p.N) {
+    uint4* dst = reinterpret_cast<uint4*>(p.C + (size_t)row * p.ldc + col0);
+    if (EPI == EPI_GATED_RESIDUAL) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        if (col0 + v * 8 < p.N) {
+          const uint32_t xs[4] = {in.x[v].x, in.x[v].y, in.x[v].z, in.x[v].w};
+          const uint32_t gs[4] = {in.g[v].x, in.g[v].y, in.g[v].z, in.g[v].w};
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = v * 8 + e * 2;
+            const float a0 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[i])));
+            const float a1 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[i + 1])));
+            w[e] = pack_bf16x2(fmaf(bf16_lo(gs[e]), a0, bf16_lo(xs[e])), fmaf(bf16_hi(gs[e]), a1, bf16_hi(xs[e])));
+          }
+          dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        if (col0 + v * 8 < p.N) {
+          dst[v] = make_uint4(pack_bf16x2(__uint_as_float(r[v * 8 + 0]), __uint_as_float(r[v * 8 + 1])),
+                              pack_bf16x2(__uint_as_float(r[v * 8 + 2]), __uint_as_float(r[v * 8 + 3])),
+                              pack_bf16x2(__uint_as_float(r[v * 8 + 4]), __uint_as_float(r[v * 8 + 5])),
+                              pack_bf16x2(__uint_as_float(r[v * 8 + 6]), __uint_as_float(r[v * 8 + 7])));
+        }
+      }
+    }
+  }
+}
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -83,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_n = (EPI == EPI_SILU_GATE) ? (p.N / (BN / 2)) : (p.N + BN - 1) / BN;
   const int num_tiles = num_m * num_n;
   const int kblocks = p.K / BK;
+  const Schedule sched(num_tiles, kblocks, kStreamK<EPI> ? p.sk_tiles : 0);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -90,10 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int mb = tile % num_m;
-        const int nb = tile / num_m;
-        for (int kb = 0; kb < kblocks; ++kb) {
+      Work w;
+      for (int idx = 0, r; ok && (r = sched.get(idx, w)) >= 0; ++idx) {
+        if (r == 0) continue;
+        const int mb = w.tile % num_m;
+        const int nb = w.tile / num_m;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, DEV_TIMEOUT_GEMM + 1)) {
             ok = false;
             break;
@@ -130,11 +268,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+    Work w;
+    for (int idx = 0, r; ok && (r = sched.get(idx, w)) >= 0; ++idx) {
+      if (r == 0) continue;
       if (!mbar_wait_warp(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, DEV_TIMEOUT_GEMM + 3)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = w.kb0; kb < w.kb1; ++kb) {
         if (!mbar_wait_warp(&full[stage], phase, abort_flag, p.err, DEV_TIMEOUT_GEMM + 4)) {
           ok = false;
           break;
@@ -145,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
           // K slice k starts 32 bytes further along the swizzled row (descriptor units: 16 bytes)
-          tc_mma_ss_warp(d_tmem, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          tc_mma_ss_warp(d_tmem, ad + 2u * k, bd + 2u * k, idesc, (kb > w.kb0 || k != 0) ? 1u : 0u);
         }
         tc_commit_warp(&empty[stage]);
         if (++stage == STAGES) {
@@ -168,14 +308,122 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int mb = tile % num_m;
-      const int nb = tile / num_m;
-      if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, p.err, DEV_TIMEOUT_GEMM + 5)) break;
-      tc_fence_after();
+    Work w;
+    for (int idx = 0, rr; (rr = sched.get(idx, w)) >= 0; ++idx) {
+      if (rr == 0) continue;
+      const int mb = w.tile % num_m;
+      const int nb = w.tile / num_m;
       const int row = mb * BM + r_in_tile;
       const bool row_ok = row < p.M;
+      if (EPI == EPI_GATED_RESIDUAL && row_ok) {
+        // the residual row segment of this tile into L2 while the main loop still runs, so the
+        // epilogue's reads do not each wait for HBM
+        const __nv_bfloat16* xr = p.resid + (size_t)row * p.ldr + nb * BN;
+#pragma unroll
+        for (int k = 0; k < BN / 64; ++k)
+          if (nb * BN + k * 64 < p.N) asm volatile("prefetch.global.L2 [%0];" ::"l"(xr + k * 64));
+      }
+      if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, p.err, DEV_TIMEOUT_GEMM + 5)) break;
+      tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      if (kStreamK<EPI> && w.slot >= 0) {
+        // ---- part of a tail tile: fp32 partial sums of this warp's 32 rows to its scratch slot,
+        // laid out as [64 groups of 4 columns][128 rows][4], so that the 32 lanes (consecutive
+        // rows) of each 16-byte store write 512 contiguous bytes
+        float4* part = reinterpret_cast<float4*>(p.sk_partial + (size_t)w.slot * BM * BN) + r_in_tile;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(t_row + c * 32, v);
+          tmem_ld_wait();
+          if (row_ok) {
+            float4* dst = part + (size_t)c * 8 * BM;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              __stcg(dst + i * BM, make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                               __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+          }
+        }
+        // count this warp's k-blocks into the arrival counter of its quarter of the tile, the
+        // writes above made visible device-wide first
+        __threadfence();
+        __syncwarp();
+        int* cnt = p.sk_count + 4 * w.tail + q;
+        int prev = 0;
+        if (lane == 0) prev = atomicAdd(cnt, w.kb1 - w.kb0);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev + (w.kb1 - w.kb0) == kblocks) {
+          // the last part to arrive: add the other parts (from scratch) and this one (from TMEM)
+          // in CTA order, then run the epilogue
+          __threadfence();
+          const long long U = (long long)p.sk_tiles * kblocks;
+          const int b_first = sk_owner((long long)w.tail * kblocks, U, gridDim.x);
+          const int b_last = sk_owner((long long)(w.tail + 1) * kblocks - 1, U, gridDim.x);
+          const int me = (int)blockIdx.x;
+          if (b_last - b_first > 2 && lane == 0) atomicCAS(p.err, 0, DEV_SCHEDULE_GEMM);  // not a host plan
+          const float4* src[2] = {nullptr, nullptr};
+          int n_other = 0;
+          for (int pb = b_first; pb <= b_last && pb <= b_first + 2; ++pb) {
+            if (pb == me) continue;
+            const int first_tail = (int)((U * pb / gridDim.x) / kblocks);
+            const int slot = 2 * pb + (w.tail == first_tail ? 0 : 1);
+            src[n_other++] = reinterpret_cast<const float4*>(p.sk_partial + (size_t)slot * BM * BN) + r_in_tile;
+          }
+          const int my_pos = me - b_first;  // where this CTA's part falls in the order
+          const int bb = row_ok ? row / p.seq : 0;
+          // n_other and my_pos are the same for the whole warp, so every lane takes the same path
+          // to the TMEM reads; row_ok only guards memory accesses.  Columns 4i..4i+3 of a chunk
+          // are i * BM float4 past the chunk's first group.  Each chunk issues all its loads (the
+          // other parts, the residual and the gate) before the TMEM read, so it waits for memory
+          // once.
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float4 x0[8], x1[8];
+            ChunkIn in;
+            if (row_ok) {
+              const float4* s0 = src[0] + (size_t)c * 8 * BM;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) x0[i] = __ldcg(s0 + i * BM);
+              if (n_other > 1) {
+                const float4* s1 = src[1] + (size_t)c * 8 * BM;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x1[i] = __ldcg(s1 + i * BM);
+              }
+              load_chunk_in<EPI>(p, row, bb, nb * BN + c * 32, in);
+            }
+            uint32_t v[32];
+            tmem_ld32(t_row + c * 32, v);
+            tmem_ld_wait();
+            if (row_ok) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float a0[4] = {x0[i].x, x0[i].y, x0[i].z, x0[i].w};
+                const float a1[4] = {x1[i].x, x1[i].y, x1[i].z, x1[i].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  // two parts add the same in either order; three add as (first + second) + third
+                  const float own = __uint_as_float(v[4 * i + e]);
+                  float t;
+                  if (n_other == 1) t = own + a0[e];
+                  else if (my_pos == 0) t = (own + a0[e]) + a1[e];
+                  else if (my_pos == 1) t = (a0[e] + own) + a1[e];
+                  else t = (a0[e] + a1[e]) + own;
+                  v[4 * i + e] = __float_as_uint(t);
+                }
+              }
+              store_chunk<EPI>(p, v, row, nb * BN + c * 32, in);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+        continue;
+      }
       if (EPI == EPI_SILU_GATE) {
         constexpr int HALF = BN / 2;
 #pragma unroll 1
@@ -269,56 +517,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = row_ok ? row / p.seq : 0;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
+          ChunkIn in;  // loaded before the TMEM read: one wait for memory per chunk
+          if (row_ok) load_chunk_in<EPI>(p, row, b, nb * BN + c * 32, in);
           uint32_t r[32];
           tmem_ld32(t_row + c * 32, r);
           tmem_ld_wait();
-          const int col0 = nb * BN + c * 32;
-          if (EPI == EPI_STORE_F32) {
-            if (row_ok && col0 < p.N) {
-              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.C) + (size_t)row * p.ldc + col0);
-#pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                if (col0 + v * 4 < p.N)
-                  dst[v] = make_float4(__uint_as_float(r[v * 4 + 0]), __uint_as_float(r[v * 4 + 1]),
-                                       __uint_as_float(r[v * 4 + 2]), __uint_as_float(r[v * 4 + 3]));
-              }
-            }
-          } else if (row_ok && col0 < p.N) {
-            uint4* dst = reinterpret_cast<uint4*>(p.C + (size_t)row * p.ldc + col0);
-            if (EPI == EPI_GATED_RESIDUAL) {
-              const uint4* xr = reinterpret_cast<const uint4*>(p.resid + (size_t)row * p.ldr + col0);
-              const uint4* gr = reinterpret_cast<const uint4*>(p.gate + (size_t)b * p.gate_bstride + col0);
-#pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                if (col0 + v * 8 < p.N) {
-                  const uint4 xv = xr[v];
-                  const uint4 gv = __ldg(gr + v);
-                  const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-                  const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
-                  uint32_t w[4];
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    const int i = v * 8 + e * 2;
-                    const float a0 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[i])));
-                    const float a1 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[i + 1])));
-                    w[e] = pack_bf16x2(fmaf(bf16_lo(gs[e]), a0, bf16_lo(xs[e])),
-                                       fmaf(bf16_hi(gs[e]), a1, bf16_hi(xs[e])));
-                  }
-                  dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-              }
-            } else {
-#pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                if (col0 + v * 8 < p.N) {
-                  dst[v] = make_uint4(pack_bf16x2(__uint_as_float(r[v * 8 + 0]), __uint_as_float(r[v * 8 + 1])),
-                                      pack_bf16x2(__uint_as_float(r[v * 8 + 2]), __uint_as_float(r[v * 8 + 3])),
-                                      pack_bf16x2(__uint_as_float(r[v * 8 + 4]), __uint_as_float(r[v * 8 + 5])),
-                                      pack_bf16x2(__uint_as_float(r[v * 8 + 6]), __uint_as_float(r[v * 8 + 7])));
-                }
-              }
-            }
-          }
+          if (row_ok) store_chunk<EPI>(p, r, row, nb * BN + c * 32, in);
         }
       }
       tc_fence_before();
@@ -340,8 +544,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+constexpr long long kSkFixupKblocks = 64;
+
+// Bytes of the arrival counters at the start of the stream-K scratch (then the partial slots):
+// four per tail tile, and there are fewer than twice as many tail tiles as CTAs.
+size_t sk_count_bytes(int grid) { return ((size_t)8 * grid * sizeof(int) + 1023) & ~(size_t)1023; }
+
+// Stream-K plan of an M x N x K launch with num_sms SMs: returns the number of tail tiles (0: the
+// plain schedule) and sets *grid.  With at least one full wave, the tail is the last full wave plus
+// the remainder on all SMs; with fewer tiles than SMs, every tile, on twice as many CTAs (at most
+// the SM count).  The fix-up of a split tile (its partial sums written, then read back and added
+// by the last CTA, each at the memory latency of a loaded GPU) costs about as much time as 64
+// k-blocks of the main loop, measured on the block's out and down projections; the tail is used
+// only when it saves more k-blocks than that.
+int sk_plan(int M, int N, int K, int num_sms, int bn, int* grid) {
+  const int tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+  const long long kb = K / BK;
+  int g, sk;
+  long long old_t, new_t;
+  if (tiles >= num_sms) {
+    const int full = tiles / num_sms, rem = tiles % num_sms;
+    if (rem == 0) return 0;
+    g = num_sms;
+    sk = num_sms + rem;
+    old_t = (full + 1) * kb;
+    new_t = (full - 1) * kb + (sk * kb + g - 1) / g + 2;
+  } else {
+    g = 2 * tiles < num_sms ? 2 * tiles : num_sms;
+    sk = tiles;
+    old_t = kb;
+    new_t = (sk * kb + g - 1) / g + 2;
+  }
+  if (old_t - new_t < kSkFixupKblocks) return 0;
+  *grid = g;
+  return sk;
+}
+
 template <int BN, int EPI>
-cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int num_sms,
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a_in, int num_sms,
                         cudaStream_t s) {
   using L = GemmSmem<BN>;
   auto kern = gemm_bf16_tn_kernel<BN, EPI>;
@@ -355,15 +595,38 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
+  GemmArgs a = a_in;
   const int num_m = (a.M + BM - 1) / BM;
   const int num_n = (EPI == EPI_SILU_GATE) ? (a.N / (BN / 2)) : (a.N + BN - 1) / BN;
   const int tiles = num_m * num_n;
-  const int grid = tiles < num_sms ? tiles : num_sms;
+  int grid = tiles < num_sms ? tiles : num_sms;
+  a.sk_tiles = 0;
+  a.sk_count = nullptr;
+  a.sk_partial = nullptr;
+  if (kStreamK<EPI> && a.sk_scratch != nullptr) {
+    int g = 0;
+    const int t = sk_plan(a.M, a.N, a.K, num_sms, BN, &g);
+    if (t > 0) {
+      grid = g;
+      a.sk_tiles = t;
+      a.sk_count = static_cast<int*>(a.sk_scratch);
+      a.sk_partial = reinterpret_cast<float*>(static_cast<uint8_t*>(a.sk_scratch) + sk_count_bytes(num_sms));
+      e = cudaMemsetAsync(a.sk_count, 0, sk_count_bytes(num_sms), s);
+      if (e != cudaSuccess) return e;
+    }
+  }
   kern<<<grid, kThreads, L::TOTAL, s>>>(ta, tb, a);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+size_t gemm_sk_scratch_bytes(int epi, int M, int N, int K, int num_sms) {
+  if (!(epi == EPI_STORE || epi == EPI_GATED_RESIDUAL || epi == EPI_STORE_F32)) return 0;
+  int g = 0;
+  if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0 || sk_plan(M, N, K, num_sms, 256, &g) == 0) return 0;
+  return sk_count_bytes(num_sms) + (size_t)2 * num_sms * BM * 256 * sizeof(float);
+}
 
 cudaError_t gemm_launch(int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int num_sms,
                         cudaStream_t s) {

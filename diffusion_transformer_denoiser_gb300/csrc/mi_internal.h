@@ -42,10 +42,19 @@ struct GemmArgs {
   int hidden;                  // H (q columns [0, H), k columns [H, 2H))
   int heads;
   float eps;
+  // Stream-K tail (EPI_STORE, EPI_GATED_RESIDUAL, EPI_STORE_F32): scratch of gemm_sk_scratch_bytes()
+  // bytes (256-byte aligned) or null, which keeps the plain persistent schedule.  The launcher fills
+  // in the three fields below.
+  void* sk_scratch;
+  int* sk_count;               // [8 * SMs] arrival counters (one per 32-row quarter of a tail tile)
+  float* sk_partial;           // [2 * SMs][256 columns][128 rows] fp32 partial tiles, two slots per CTA
+  int sk_tiles;                // tiles on the stream-K tail (0: none)
 };
 
 cudaError_t gemm_launch(int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int num_sms,
                         cudaStream_t s);
+// Scratch bytes the stream-K tail of this GEMM needs (0 when the plain schedule is used for it).
+size_t gemm_sk_scratch_bytes(int epi, int M, int N, int K, int num_sms);
 
 struct AttnArgs {
   int batch, seq, n_heads;

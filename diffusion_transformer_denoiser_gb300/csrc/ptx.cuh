@@ -18,6 +18,7 @@ enum : int {
   DEV_TIMEOUT_GEMM = 0x100,
   DEV_TIMEOUT_ATTN = 0x200,
   DEV_TIMEOUT_SELFTEST = 0x300,
+  DEV_SCHEDULE_GEMM = 0x400,  // a GEMM launch whose stream-K plan the kernel cannot carry out
 };
 
 // Wall-clock limit of a single wait (ns).  No legitimate wait in these kernels lasts more than a

@@ -64,10 +64,12 @@ mi_status mi_device_supported(void);
 mi_status mi_device_error(int* code);
 
 /* Error codes mi_device_error reports: 0x100 + k (a GEMM wait), 0x200 + k (an attention wait),
- * 0x300 (the self-test below). */
+ * 0x300 (the self-test below), 0x400 (a GEMM whose split of tail tiles over the CTAs has more parts
+ * per tile than its fix-up adds; the library's own plans never produce one). */
 #define MI_DEV_TIMEOUT_GEMM 0x100
 #define MI_DEV_TIMEOUT_ATTN 0x200
 #define MI_DEV_TIMEOUT_SELFTEST 0x300
+#define MI_DEV_SCHEDULE_GEMM 0x400
 
 /* Enqueues a one-CTA kernel whose pipeline wait can never complete: the wait gives up after
  * limit_us microseconds (at most 1e6), records MI_DEV_TIMEOUT_SELFTEST in the device error flag and

@@ -100,6 +100,20 @@ def test_block_parity_full_size(name):
     _check_all(gb, oracle_block(name), True)
 
 
+def test_fused_and_unfused_give_identical_bytes_on_the_stream_k_tail():
+    # at this geometry (8260 rows) the down projection splits its last full wave and remainder of
+    # tiles along k over all SMs in both paths; the partial sums are added in a fixed order, so the
+    # two paths still agree exactly, and so do repeats
+    mi = require_gpu()
+    inp = mi_synth.block_inputs(mi_synth.GEOMETRIES["block_1024_cfg_b2"], 3)
+    a = GpuBlock(mi, inp, True)
+    b = GpuBlock(mi, inp, False)
+    ya = a.run().clone()
+    assert torch.equal(ya.view(torch.int16), b.run().view(torch.int16))
+    assert torch.equal(ya.view(torch.int16), a.run().view(torch.int16))
+    assert mi.device_error() == 0
+
+
 def test_block_repeats_bit_for_bit():
     # the same block twice, with another geometry run in between, gives identical bytes
     mi = require_gpu()
