@@ -83,6 +83,7 @@ _SIGNATURES = {
     "mi_model_init": ([ctypes.POINTER(_P), ctypes.POINTER(_ModelDesc)], _I),
     "mi_model_destroy": ([_P], None),
     "mi_model_workspace_size": ([_P, ctypes.POINTER(SeqLayout), ctypes.POINTER(_SZ)], _I),
+    "mi_model_plan": ([_P, ctypes.POINTER(SeqLayout), _I, _SZ, ctypes.POINTER(_SZ), ctypes.POINTER(ctypes.c_uint8)], _I),
     "mi_denoise_step": ([_P, ctypes.POINTER(SeqLayout), _P, _P, _P, _P, _P, _P, _I, _P, _F, _F, _P, _P, _SZ,
                          _P], _I),
     "mi_rope_tables": ([_I, _I, _I, _F, _P, _P, _P], _I),
@@ -243,6 +244,15 @@ class Model:
         n = _SZ(0)
         _check(lib().mi_model_workspace_size(self.handle, ctypes.byref(layout), ctypes.byref(n)))
         return n.value
+
+    def plan(self, layouts: Sequence[SeqLayout], budget_bytes: int):
+        """One workspace for several layouts: (bytes, served flags); MiError(status 3) when none fits."""
+        n = len(layouts)
+        arr = (SeqLayout * n)(*layouts)
+        flags = (ctypes.c_uint8 * n)()
+        nb = _SZ(0)
+        _check(lib().mi_model_plan(self.handle, arr, n, budget_bytes, ctypes.byref(nb), flags))
+        return nb.value, [bool(f) for f in flags]
 
     def denoise_step(self, layout: SeqLayout, latent, text_rows, mods, mod_final, rope_cos, rope_sin, key_mask,
                      dt: float, guidance: float, ws, skip_neg=None, rope_bstride: int = 0, stream=None):

@@ -581,6 +581,30 @@ mi_status mi_model_workspace_size(const mi_model* model, const mi_seq_layout* L,
   return MI_OK;
 }
 
+mi_status mi_model_plan(const mi_model* model, const mi_seq_layout* layouts, int n, size_t budget_bytes,
+                        size_t* bytes, uint8_t* served) {
+  if (!model || !layouts || !bytes) return fail(MI_ERR_INVALID_ARG, "null argument");
+  if (n < 1) return fail(MI_ERR_INVALID_ARG, "plan needs at least one layout (n=%d)", n);
+  size_t most = 0;
+  int n_served = 0;
+  for (int i = 0; i < n; ++i) {
+    int S = 0;
+    mi_status st = check_layout(&layouts[i], &S);
+    if (st != MI_OK) return st;
+    const size_t need = plan_step(model, layouts[i].batch, S, layouts[i].grid_h * layouts[i].grid_w).total;
+    const bool ok = need <= budget_bytes;
+    if (served) served[i] = ok ? 1 : 0;
+    if (ok) {
+      ++n_served;
+      if (need > most) most = need;
+    }
+  }
+  *bytes = most;
+  if (n_served == 0)
+    return fail(MI_ERR_WORKSPACE, "out of device memory: none of the %d layouts fits in %zu bytes", n, budget_bytes);
+  return MI_OK;
+}
+
 mi_status mi_denoise_step(mi_model* model, const mi_seq_layout* L, void* latent, const void* text_rows,
                           const void* mods, const void* mod_final, const float* rope_cos, const float* rope_sin,
                           int rope_bstride, const uint8_t* key_mask, float dt, float guidance,

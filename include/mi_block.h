@@ -188,6 +188,24 @@ void mi_model_destroy(mi_model* model);
 mi_status mi_model_workspace_size(const mi_model* model, const mi_seq_layout* L, size_t* bytes);
 
 /*
+ * One planned workspace for several geometries (PR #2281 "What this changes": the host plans one
+ * scratch and serves every geometry inside it; "Measured": a picture whose scratch does not fit is
+ * refused with an out-of-memory status and the engine keeps serving, returning the same bytes for
+ * the next request).  For each of the n layouts, its need is mi_model_workspace_size; a layout is
+ * served when its need is at most budget_bytes.
+ *   layouts  HOST array of n layouts (n >= 1)
+ *   bytes    out: the largest need among the served layouts (0 when none is served)
+ *   served   HOST uint8 [n] or NULL, out: 1 for a served layout, 0 for a refused one
+ * Returns MI_OK when at least one layout is served, MI_ERR_WORKSPACE (the out-of-memory refusal)
+ * when none is, MI_ERR_INVALID_ARG for a bad layout.  One workspace of *bytes then serves every
+ * served layout in mi_denoise_step, in any order; a step whose layout needs more than the
+ * workspace it is given is refused with MI_ERR_WORKSPACE before anything is enqueued, and the
+ * model, its workspace and the stream stay usable.  Host arithmetic only: nothing is enqueued.
+ */
+mi_status mi_model_plan(const mi_model* model, const mi_seq_layout* layouts, int n, size_t budget_bytes,
+                        size_t* bytes, uint8_t* served);
+
+/*
  * One guided denoising step (PR #2281 "What this changes": the pipeline's schedule and
  * classifier-free guidance with an empty negative prompt; PR #1528 "Measured": Euler steps):
  *   u = latent W_in^T;  x_b = [text_rows_b ; u];  x_b <- every block;

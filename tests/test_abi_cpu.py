@@ -81,6 +81,7 @@ def test_null_arguments(lib):
     assert lib.mi_block_init(None, None) == 1
     assert lib.mi_block_forward(None, None, None, None, None, None, None, 0, None, None, 0, None) == 1
     assert lib.mi_gemm_bf16(None, None, None, 4, 8, 64, None) == 1
+    assert lib.mi_model_plan(None, None, 1, 0, None, None) == 1
 
 
 def test_gemm_shape_refusal(lib):
