@@ -34,6 +34,8 @@ METRIC = "image tokens/s per DiT block fwd (1 GB300); attn+GEMM TFLOP/s as % bf1
 UNIT = "image tokens/s"
 WORKLOAD = "block_1024"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# nominal GB300 figures, reported beside the measured ones (which stay the primary denominators)
+NOMINAL_PEAKS = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 
 
 def load_peaks():
@@ -357,9 +359,12 @@ def run_ours(args):
             "data": "synthetic: seeded N(0,1) activations, N(0,0.02) weights, N(0,0.1) modulation",
             "config": config_of(g),
             "attn_gemm_tflops": tflops, "pct_bf16_peak": tflops / peak,
+            "pct_bf16_nominal": tflops / NOMINAL_PEAKS["bf16_tflops"],
             "roofline": {"bound": "tensor", "kernel": "gemm_gate_up_silu (tcgen05, fused SiLU gate)",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                          "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
+                         "peak_nominal": NOMINAL_PEAKS["bf16_tflops"],
+                         "frac_nominal": achieved / NOMINAL_PEAKS["bf16_tflops"],
                          "traffic": traffic},
             "kernels": {k: {"ms": v["ms"], **{kk: vv for kk, vv in v.items() if kk != "ms"}} for k, v in kern.items()},
             "cpu_baseline": None,
@@ -489,9 +494,11 @@ def extras(mi, torch, devc, stream):
     return out
 
 
-def kernel_times(mi, torch, g, inp, t, devc, stream, reps):
-    """Average device time of each kernel of the block, launched alone on the bench stream with CUDA
-    events around `reps` back-to-back launches, at the workload's shapes."""
+def kernel_times(mi, torch, g, inp, t, devc, stream, reps, hbm_reps=100):
+    """Device time of each kernel of the block, launched alone on the bench stream at the workload's
+    shapes.  Tensor-bound kernels: CUDA events around a CUDA graph of `reps` back-to-back launches
+    (the average).  HBM-bound kernels: the median of `hbm_reps` single launches, each with CUDA events
+    around it and L2 flushed before it (a 256 MB write, more than the 129 MB L2)."""
     R, H, I, nh, S, B = g.rows, g.hidden, g.mlp_inter, g.n_heads, g.seq, g.batch
     bf = torch.bfloat16
     w = inp.weights
@@ -535,11 +542,30 @@ def kernel_times(mi, torch, g, inp, t, devc, stream, reps):
                                      {"flops": 2.0 * R * H * I}),
     }
     peaks, _ = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=devc)
     out = {}
     for name, (fn, work) in calls.items():
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
+        if "bytes" in work:
+            gstream = torch.cuda.current_stream()
+            evs = []
+            for _ in range(hbm_reps):
+                flush.zero_()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(gstream)
+                fn()
+                b.record(gstream)
+                evs.append((a, b))
+            torch.cuda.synchronize()
+            ms = float(np.median([a.elapsed_time(b) for a, b in evs]))
+            gbs = work["bytes"] / (ms * 1e-3) / 1e9
+            out[name] = {"ms": ms, "gbs": gbs, "frac_hbm_peak": gbs / peaks["hbm_gbs"],
+                         "frac_hbm_nominal": gbs / NOMINAL_PEAKS["hbm_gbs"],
+                         "timing": f"median of {hbm_reps} single launches, L2 flushed before each"}
+            continue
         # capture the launches in a CUDA graph so host launch overhead does not hide in the timing
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
@@ -557,12 +583,10 @@ def kernel_times(mi, torch, g, inp, t, devc, stream, reps):
         ms = e0.elapsed_time(e1) / reps
         del graph
         ent = {"ms": ms}
-        if "flops" in work:
-            ent["tflops"] = work["flops"] / (ms * 1e-3) / 1e12
-            ent["frac_bf16_peak"] = ent["tflops"] / peaks["bf16_tflops"]
-        else:
-            ent["gbs"] = work["bytes"] / (ms * 1e-3) / 1e9
-            ent["frac_hbm_peak"] = ent["gbs"] / peaks["hbm_gbs"]
+        ent["tflops"] = work["flops"] / (ms * 1e-3) / 1e12
+        ent["frac_bf16_peak"] = ent["tflops"] / peaks["bf16_tflops"]
+        ent["frac_bf16_nominal"] = ent["tflops"] / NOMINAL_PEAKS["bf16_tflops"]
+        ent["timing"] = f"average of a CUDA graph of {reps} back-to-back launches"
         out[name] = ent
     return out
 

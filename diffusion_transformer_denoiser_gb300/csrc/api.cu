@@ -139,7 +139,9 @@ bool encode_4d_bf16(CUtensorMap* m, const void* base, const uint64_t dims[4], co
 // ------------------------------------------------------------------------------ GEMM helper
 namespace {
 
-constexpr int kGemmBN = 256;
+// Every W operand map has 128-row boxes: the one-CTA GEMM loads a 256-row W tile as two boxes and
+// each CTA of a pair loads one.
+constexpr int kWBox = 128;
 
 // A operand map: [rows, k] row-major, box 64 x 128.
 bool map_a(CUtensorMap* m, const void* a, int rows, int k) {
@@ -185,7 +187,7 @@ mi::GemmArgs gemm_args(int m, int n, int k, void* c, int* err) {
 // ------------------------------------------------------------------------------ block
 struct mi_block {
   mi_block_desc d;
-  CUtensorMap tm_wqkv, tm_wo, tm_wgu, tm_wgu_split, tm_wd;
+  CUtensorMap tm_wqkv, tm_wo, tm_wgu, tm_wd;
   int dev;
   int num_sms;
 };
@@ -360,7 +362,7 @@ static mi_status block_forward_impl(mi_block* blk, int batch, int S, const void*
   // 7. gate/up projection + SiLU gate
   if (d.fuse_epilogues) {
     mi::GemmArgs g = gemm_args(R, I, H, m, dev->err);
-    mi_status st = run_gemm(dev, mi::EPI_SILU_GATE, tm_h2, blk->tm_wgu_split, g, s);
+    mi_status st = run_gemm(dev, mi::EPI_SILU_GATE, tm_h2, blk->tm_wgu, g, s);
     if (st != MI_OK) return st;
   } else {
     mi::GemmArgs g = gemm_args(R, 2 * I, H, gu, dev->err);
@@ -440,9 +442,8 @@ mi_status mi_block_init(mi_block** out, const mi_block_desc* desc) {
   b->num_sms = dev->num_sms;
   MI_CUDA(cudaGetDevice(&b->dev), "cudaGetDevice");
   const int H = desc->hidden, I = desc->mlp_inter;
-  if (!map_w(&b->tm_wqkv, desc->w_qkv, 3 * H, H, kGemmBN) || !map_w(&b->tm_wo, desc->w_o, H, H, kGemmBN) ||
-      !map_w(&b->tm_wgu, desc->w_gu, 2 * I, H, kGemmBN) ||
-      !map_w(&b->tm_wgu_split, desc->w_gu, 2 * I, H, kGemmBN / 2) || !map_w(&b->tm_wd, desc->w_d, H, I, kGemmBN)) {
+  if (!map_w(&b->tm_wqkv, desc->w_qkv, 3 * H, H, kWBox) || !map_w(&b->tm_wo, desc->w_o, H, H, kWBox) ||
+      !map_w(&b->tm_wgu, desc->w_gu, 2 * I, H, kWBox) || !map_w(&b->tm_wd, desc->w_d, H, I, kWBox)) {
     delete b;
     return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed (weights)");
   }
@@ -557,8 +558,8 @@ mi_status mi_model_init(mi_model** out, const mi_model_desc* desc) {
     }
     m->blocks.push_back(b);
   }
-  if (!map_w(&m->tm_win, m->w_in, m->hidden, m->latent_ch, kGemmBN) ||
-      !map_w(&m->tm_wout, m->w_out, m->latent_ch, m->hidden, kGemmBN)) {
+  if (!map_w(&m->tm_win, m->w_in, m->hidden, m->latent_ch, kWBox) ||
+      !map_w(&m->tm_wout, m->w_out, m->latent_ch, m->hidden, kWBox)) {
     mi_model_destroy(m);
     return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed (embedders)");
   }
@@ -710,8 +711,8 @@ static mi_status gemm_common(int epi, const void* a, const void* w, void* c, int
   if (st != MI_OK) return st;
   CUtensorMap ta, tb;
   const int w_rows = epi == mi::EPI_SILU_GATE ? 2 * n : n;
-  const int box = epi == mi::EPI_SILU_GATE ? kGemmBN / 2 : kGemmBN;
-  if (!map_a(&ta, a, m, k) || !map_w(&tb, w, w_rows, k, box)) return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed");
+  if (!map_a(&ta, a, m, k) || !map_w(&tb, w, w_rows, k, kWBox))
+    return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed");
   mi::GemmArgs g = gemm_args(m, n, k, c, dev->err);
   if (epi == mi::EPI_GATED_RESIDUAL) {
     if (!resid || !mod) return fail(MI_ERR_INVALID_ARG, "null resid or mod");
@@ -758,7 +759,7 @@ mi_status mi_gemm_bf16_qkv_rope(const void* a, const void* w_qkv, const void* q_
   st = require_sm103(&dev);
   if (st != MI_OK) return st;
   CUtensorMap ta, tb;
-  if (!map_a(&ta, a, m, H) || !map_w(&tb, w_qkv, 3 * H, H, kGemmBN)) return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed");
+  if (!map_a(&ta, a, m, H) || !map_w(&tb, w_qkv, 3 * H, H, kWBox)) return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed");
   mi::GemmArgs g = gemm_args(m, 3 * H, H, qkv_v, dev->err);
   g.seq = seq;
   g.qp = mb(qp);
@@ -948,8 +949,8 @@ mi_status mi_tmod_init(mi_tmod** out, const mi_tmod_desc* desc) {
   if (!m) return fail(MI_ERR_INVALID_ARG, "host allocation failed");
   m->d = *desc;
   const int H = desc->hidden;
-  if (!map_w(&m->tm_w1, desc->w_t1, H, kTDim, kGemmBN) || !map_w(&m->tm_w2, desc->w_t2, H, H, kGemmBN) ||
-      !map_w(&m->tm_wmod, desc->w_mod, (6 * desc->n_blocks + 2) * H, H, kGemmBN)) {
+  if (!map_w(&m->tm_w1, desc->w_t1, H, kTDim, kWBox) || !map_w(&m->tm_w2, desc->w_t2, H, H, kWBox) ||
+      !map_w(&m->tm_wmod, desc->w_mod, (6 * desc->n_blocks + 2) * H, H, kWBox)) {
     delete m;
     return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed (timestep weights)");
   }

@@ -19,6 +19,8 @@
 // counts its k-blocks into the tile's arrival counter; the CTA whose count completes the tile adds
 // the other parts to its own (still in TMEM) in CTA order, a fixed order, so results still repeat
 // bit for bit, and runs the epilogue.  Nobody waits for another CTA: no co-residency is assumed.
+#include <stdlib.h>
+
 #include "mi_internal.h"
 #include "ptx.cuh"
 
@@ -168,6 +170,114 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& p, const uint32_t (&
   }
 }
 
+// Epilogue of one tile for the row of TMEM lane (t_row's lane base + lane): the fused element-wise
+// tail of each epilogue applied to the fp32 sums, then the single store.  Shared by the one-CTA and
+// the CTA-pair kernels (row: this thread's output row; nb: the tile's column block).
+template <int BN, int EPI>
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& p, uint32_t t_row, int row, bool row_ok, int nb) {
+  if (EPI == EPI_SILU_GATE) {
+    constexpr int HALF = BN / 2;
+#pragma unroll 1
+    for (int c = 0; c < HALF / 32; ++c) {
+      uint32_t g[32], u[32];
+      tmem_ld32(t_row + c * 32, g);
+      tmem_ld32(t_row + HALF + c * 32, u);
+      tmem_ld_wait();
+      if (row_ok) {
+        const int col0 = nb * HALF + c * 32;
+        uint4* dst = reinterpret_cast<uint4*>(p.C + (size_t)row * p.ldc + col0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = v * 8 + e * 2;
+            // round the GEMM outputs to bf16 first, as the unfused path stores them
+            const float g0 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(g[i])));
+            const float g1 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(g[i + 1])));
+            const float u0 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(u[i])));
+            const float u1 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(u[i + 1])));
+            w[e] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
+          }
+          dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+  } else if (EPI == EPI_QKV_ROPE && nb * BN < 2 * p.hidden) {
+    // q or k columns: the tile holds two whole heads of this row.  Per head: round the sums to
+    // bf16 (the QKV projection's rounding point), RMSNorm over the 128 values with the gain,
+    // rotate the pairs (2p, 2p+1) by the row's angles, and write the packed head row.  The
+    // reductions follow the stand-alone q/k kernel's order exactly (sixteen 8-element fma
+    // chains combined by the same butterfly), so fused and unfused results are identical.
+    const int which = nb * BN >= p.hidden ? 1 : 0;
+    const int head0 = (nb * BN - which * p.hidden) / kHeadDim;
+    const __nv_bfloat16* gain = which ? p.wk : p.wq;
+    __nv_bfloat16* dst_base = which ? p.kp : p.qp;
+    const int b = row_ok ? row / p.seq : 0;
+    const int s = row_ok ? row % p.seq : 0;
+#pragma unroll 1
+    for (int hh = 0; hh < BN / kHeadDim; ++hh) {
+      uint32_t r[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(t_row + hh * kHeadDim + c * 32, r + c * 32);
+      tmem_ld_wait();
+      if (row_ok) {
+        float part[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float ss = 0.0f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float f = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[k * 8 + e])));
+            r[k * 8 + e] = __float_as_uint(f);
+            ss = fmaf(f, f, ss);
+          }
+          part[k] = ss;
+        }
+        float v8[8], w4[4];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v8[k] = part[k] + part[k + 8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w4[k] = v8[k] + v8[k + 4];
+        const float tot = (w4[0] + w4[2]) + (w4[1] + w4[3]);
+        const float rstd = rsqrtf(tot * (1.0f / kHeadDim) + p.eps);
+        const float* cr = p.rope_cos + (size_t)b * p.rope_bstride + (size_t)s * (kHeadDim / 2);
+        const float* sr = p.rope_sin + (size_t)b * p.rope_bstride + (size_t)s * (kHeadDim / 2);
+        uint4* dst = reinterpret_cast<uint4*>(
+            dst_base + (((size_t)b * p.heads + head0 + hh) * p.seq + s) * kHeadDim);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {  // 8 elements = 4 rotary pairs per 16-byte store
+          const uint4 gv = __ldg(reinterpret_cast<const uint4*>(gain) + v);
+          const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
+          const float4 c4 = __ldg(reinterpret_cast<const float4*>(cr) + v);
+          const float4 s4 = __ldg(reinterpret_cast<const float4*>(sr) + v);
+          const float cs[4] = {c4.x, c4.y, c4.z, c4.w};
+          const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
+          uint32_t w[4];
+#pragma unroll
+          for (int pr = 0; pr < 4; ++pr) {
+            const float a = __uint_as_float(r[v * 8 + 2 * pr]) * rstd * bf16_lo(gs[pr]);
+            const float bb = __uint_as_float(r[v * 8 + 2 * pr + 1]) * rstd * bf16_hi(gs[pr]);
+            w[pr] = pack_bf16x2(fmaf(a, cs[pr], -bb * sn[pr]), fmaf(a, sn[pr], bb * cs[pr]));
+          }
+          dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+  } else {
+    const int b = row_ok ? row / p.seq : 0;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      ChunkIn in;  // loaded before the TMEM read: one wait for memory per chunk
+      if (row_ok) load_chunk_in<EPI>(p, row, b, nb * BN + c * 32, in);
+      uint32_t r[32];
+      tmem_ld32(t_row + c * 32, r);
+      tmem_ld_wait();
+      if (row_ok) store_chunk<EPI>(p, r, row, nb * BN + c * 32, in);
+    }
+  }
+}
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -244,7 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sB + stage * L::B_BYTES + L::B_BYTES / 2, &tmB, &full[stage], kb * BK,
                         p.N + nb * (BN / 2));
           } else {
+            // the 256-row W tile as two 128-row boxes (W maps have 128-row boxes)
             tma_load_2d(sB + stage * L::B_BYTES, &tmB, &full[stage], kb * BK, nb * BN);
+            tma_load_2d(sB + stage * L::B_BYTES + L::B_BYTES / 2, &tmB, &full[stage], kb * BK, nb * BN + BN / 2);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -424,107 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      if (EPI == EPI_SILU_GATE) {
-        constexpr int HALF = BN / 2;
-#pragma unroll 1
-        for (int c = 0; c < HALF / 32; ++c) {
-          uint32_t g[32], u[32];
-          tmem_ld32(t_row + c * 32, g);
-          tmem_ld32(t_row + HALF + c * 32, u);
-          tmem_ld_wait();
-          if (row_ok) {
-            const int col0 = nb * HALF + c * 32;
-            uint4* dst = reinterpret_cast<uint4*>(p.C + (size_t)row * p.ldc + col0);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t w[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int i = v * 8 + e * 2;
-                // round the GEMM outputs to bf16 first, as the unfused path stores them
-                const float g0 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(g[i])));
-                const float g1 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(g[i + 1])));
-                const float u0 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(u[i])));
-                const float u1 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(u[i + 1])));
-                w[e] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
-              }
-              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
-        }
-      } else if (EPI == EPI_QKV_ROPE && nb * BN < 2 * p.hidden) {
-        // q or k columns: the tile holds two whole heads of this row.  Per head: round the sums to
-        // bf16 (the QKV projection's rounding point), RMSNorm over the 128 values with the gain,
-        // rotate the pairs (2p, 2p+1) by the row's angles, and write the packed head row.  The
-        // reductions follow the stand-alone q/k kernel's order exactly (sixteen 8-element fma
-        // chains combined by the same butterfly), so fused and unfused results are identical.
-        const int which = nb * BN >= p.hidden ? 1 : 0;
-        const int head0 = (nb * BN - which * p.hidden) / kHeadDim;
-        const __nv_bfloat16* gain = which ? p.wk : p.wq;
-        __nv_bfloat16* dst_base = which ? p.kp : p.qp;
-        const int b = row_ok ? row / p.seq : 0;
-        const int s = row_ok ? row % p.seq : 0;
-#pragma unroll 1
-        for (int hh = 0; hh < BN / kHeadDim; ++hh) {
-          uint32_t r[128];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32(t_row + hh * kHeadDim + c * 32, r + c * 32);
-          tmem_ld_wait();
-          if (row_ok) {
-            float part[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              float ss = 0.0f;
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float f = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[k * 8 + e])));
-                r[k * 8 + e] = __float_as_uint(f);
-                ss = fmaf(f, f, ss);
-              }
-              part[k] = ss;
-            }
-            float v8[8], w4[4];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v8[k] = part[k] + part[k + 8];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) w4[k] = v8[k] + v8[k + 4];
-            const float tot = (w4[0] + w4[2]) + (w4[1] + w4[3]);
-            const float rstd = rsqrtf(tot * (1.0f / kHeadDim) + p.eps);
-            const float* cr = p.rope_cos + (size_t)b * p.rope_bstride + (size_t)s * (kHeadDim / 2);
-            const float* sr = p.rope_sin + (size_t)b * p.rope_bstride + (size_t)s * (kHeadDim / 2);
-            uint4* dst = reinterpret_cast<uint4*>(
-                dst_base + (((size_t)b * p.heads + head0 + hh) * p.seq + s) * kHeadDim);
-#pragma unroll
-            for (int v = 0; v < 16; ++v) {  // 8 elements = 4 rotary pairs per 16-byte store
-              const uint4 gv = __ldg(reinterpret_cast<const uint4*>(gain) + v);
-              const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
-              const float4 c4 = __ldg(reinterpret_cast<const float4*>(cr) + v);
-              const float4 s4 = __ldg(reinterpret_cast<const float4*>(sr) + v);
-              const float cs[4] = {c4.x, c4.y, c4.z, c4.w};
-              const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
-              uint32_t w[4];
-#pragma unroll
-              for (int pr = 0; pr < 4; ++pr) {
-                const float a = __uint_as_float(r[v * 8 + 2 * pr]) * rstd * bf16_lo(gs[pr]);
-                const float bb = __uint_as_float(r[v * 8 + 2 * pr + 1]) * rstd * bf16_hi(gs[pr]);
-                w[pr] = pack_bf16x2(fmaf(a, cs[pr], -bb * sn[pr]), fmaf(a, sn[pr], bb * cs[pr]));
-              }
-              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
-        }
-      } else {
-        const int b = row_ok ? row / p.seq : 0;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          ChunkIn in;  // loaded before the TMEM read: one wait for memory per chunk
-          if (row_ok) load_chunk_in<EPI>(p, row, b, nb * BN + c * 32, in);
-          uint32_t r[32];
-          tmem_ld32(t_row + c * 32, r);
-          tmem_ld_wait();
-          if (row_ok) store_chunk<EPI>(p, r, row, nb * BN + c * 32, in);
-        }
-      }
+      epilogue_tile<BN, EPI>(p, t_row, row, row_ok, nb);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -541,6 +553,209 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, 2 * BN);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// CTA-pair kernel: a cluster of two CTAs computes 256 x 256 tiles with tcgen05 cta_group::2 MMAs.
+// Each CTA loads its own 128 rows of A and half of the 256-row W tile (64-column k-blocks), so a
+// pipeline stage holds 32 KB per CTA instead of 48 KB: six stages fit where the one-CTA kernel has
+// four, and each SM pulls a third less operand data per MMA.  The leader CTA (rank 0) issues the
+// MMAs for the pair; each CTA's epilogue drains its own 128 TMEM rows.
+//   * warp 0 of each CTA: TMA producer into its own ring.  Both CTAs' copies of a stage complete on
+//     the leader's `full` barrier (the pair form of the TMA), which the leader arms for both;
+//   * warp 1 of the leader: waits on `full`, issues the pair MMAs and commits to `empty` / `tfull`
+//     in both CTAs (multicast);
+//   * warps 2-5 of each CTA: epilogue, then an arrive on the leader's `tempty` (count 8).
+// All waits are bounded.  The leader's producer arms every stage whose release both CTAs see (its
+// wait ignores the abort flag), so its drain covers the follower's copies too; both CTAs meet at a
+// cluster barrier before TMEM is released and either exits.
+constexpr int kPairStages = 6;
+
+struct PairSmem {
+  static constexpr int A_BYTES = BM * BK * 2;   // 128 rows of A
+  static constexpr int B_BYTES = 128 * BK * 2;  // this CTA's half of the 256-row W tile
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int BAR_OFF = kPairStages * STAGE_BYTES;
+  static constexpr int TOTAL = BAR_OFF + 512 + 1024;  // barriers + alignment slack
+};
+
+template <int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmArgs p) {
+  constexpr int BN = 256;
+  using L = PairSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kPairStages * L::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);  // the leader's: both CTAs' copies
+  uint64_t* empty = full + kPairStages;
+  uint64_t* tfull = empty + kPairStages;     // [2]
+  uint64_t* tempty = tfull + 2;              // [2], leader: 4 local + 4 remote epilogue warps
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, 2 * BN);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive or multicast commit
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_pm = (p.M + 2 * BM - 1) / (2 * BM);
+  const int num_n = (EPI == EPI_SILU_GATE) ? (p.N / (BN / 2)) : (p.N + BN - 1) / BN;
+  const int num_units = num_pm * num_n;
+  const int kblocks = p.K / BK;
+  const int cid = (int)blockIdx.x >> 1;
+  const int n_clusters = (int)gridDim.x >> 1;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------------ TMA producer (both CTAs)
+      const uint32_t leader_full = cluster_addr(full, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = cid; u < num_units && ok; u += n_clusters) {
+        const int pm = u % num_pm;
+        const int nb = u / num_pm;
+        const int m0 = pm * 2 * BM + (int)rank * BM;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait_noabort<true>(&empty[stage], phase ^ 1u, abort_flag, p.err, DEV_TIMEOUT_GEMM + 11)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * L::STAGE_BYTES);
+          const uint32_t fb = leader_full + stage * 8;
+          tma_load_2d_pair(sA + stage * L::A_BYTES, &tmA, fb, kb * BK, m0);
+          if (EPI == EPI_SILU_GATE) {
+            // the leader loads the gate rows [nb*128, +128), the follower the up rows [N + nb*128, +128)
+            tma_load_2d_pair(sB + stage * L::B_BYTES, &tmB, fb, kb * BK, (int)rank * p.N + nb * (BN / 2));
+          } else {
+            tma_load_2d_pair(sB + stage * L::B_BYTES, &tmB, fb, kb * BK, nb * BN + (int)rank * 128);
+          }
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // drain (leader): every armed phase, which counts both CTAs' copies, has completed
+      if (leader) {
+        for (int s = 0; s < kPairStages; ++s) {
+          mbar_wait_drain(&full[s], (s < stage) ? phase : (phase ^ 1u), p.err, DEV_TIMEOUT_GEMM + 12);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (leader) {
+      // ------------------------------------------------------------------ MMA issuer (leader)
+      constexpr uint32_t idesc = idesc_bf16(2 * BM, BN, false, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = cid; u < num_units && ok; u += n_clusters) {
+        if (!mbar_wait_warp<true>(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, DEV_TIMEOUT_GEMM + 13)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait_warp<true>(&full[stage], phase, abort_flag, p.err, DEV_TIMEOUT_GEMM + 14)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_sw128(smem_u32(sA + stage * L::A_BYTES), 16, 1024);
+          const uint64_t bd = sdesc_sw128(smem_u32(sB + stage * L::B_BYTES), 16, 1024);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma_pair_warp(d_tmem, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          tc_commit_pair_warp(&empty[stage]);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        tc_commit_pair_warp(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      tc_commit_pair_warp(drain);
+      mbar_wait_drain<true>(drain, 0, p.err, DEV_TIMEOUT_GEMM + 16);
+    } else if (lane == 0) {
+      // follower: the leader's last commit (multicast to this CTA too) lands before this CTA exits
+      mbar_wait_drain<true>(drain, 0, p.err, DEV_TIMEOUT_GEMM + 18);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue warps (both CTAs)
+    const int q = warp & 3;
+    const int r_in_tile = q * 32 + lane;
+    const uint32_t leader_tempty = cluster_addr(tempty, 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = cid; u < num_units; u += n_clusters) {
+      const int pm = u % num_pm;
+      const int nb = u / num_pm;
+      const int row = pm * 2 * BM + (int)rank * BM + r_in_tile;
+      const bool row_ok = row < p.M;
+      if (EPI == EPI_GATED_RESIDUAL && row_ok) {
+        const __nv_bfloat16* xr = p.resid + (size_t)row * p.ldr + nb * BN;
+#pragma unroll
+        for (int k = 0; k < BN / 64; ++k)
+          if (nb * BN + k * 64 < p.N) asm volatile("prefetch.global.L2 [%0];" ::"l"(xr + k * 64));
+      }
+      if (!mbar_wait_warp<true>(&tfull[acc], acc_phase, abort_flag, p.err, DEV_TIMEOUT_GEMM + 17)) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      epilogue_tile<BN, EPI>(p, t_row, row, row_ok, nb);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(leader_tempty + acc * 8);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  __syncthreads();
+  cluster_sync();  // the pair's MMAs, commits and remote arrives are all done before either exits
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, 2 * BN);
   }
 }
 
@@ -619,6 +834,69 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
   return cudaGetLastError();
 }
 
+// MI_GEMM_PAIRS=0 keeps every GEMM on the one-CTA kernel (for comparisons).
+bool pair_disabled() {
+  static const bool off = [] {
+    const char* e = getenv("MI_GEMM_PAIRS");
+    return e && e[0] == '0';
+  }();
+  return off;
+}
+
+// Clusters of two that can be resident at once with the pair kernel's shared memory (cached per
+// device and epilogue); 0 when the query fails.
+template <int EPI>
+int pair_max_clusters(int num_sms) {
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (cache[dev] == 0) {
+    if (cudaFuncSetAttribute(gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, PairSmem::TOTAL) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = PairSmem::TOTAL;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<EPI>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+template <int EPI>
+cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int max_clusters,
+                             cudaStream_t s) {
+  const int num_pm = (a.M + 2 * BM - 1) / (2 * BM);
+  const int num_n = (EPI == EPI_SILU_GATE) ? (a.N / 128) : (a.N + 255) / 256;
+  const int units = num_pm * num_n;
+  const int clusters = units < max_clusters ? units : max_clusters;
+  gemm_pair_kernel<EPI><<<2 * clusters, kThreads, PairSmem::TOTAL, s>>>(ta, tb, a);
+  return cudaGetLastError();
+}
+
+// The pair kernel serves launches of more than one 128-row block and at least one full column tile
+// that do not take the stream-K tail; the one-CTA kernel keeps the others (a single row block, the
+// narrow velocity projection, long-k tail launches).
+template <int EPI>
+cudaError_t launch_gemm_auto(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int num_sms,
+                             cudaStream_t s) {
+  int g = 0;
+  const bool tail = kStreamK<EPI> && a.sk_scratch != nullptr && sk_plan(a.M, a.N, a.K, num_sms, 256, &g) > 0;
+  const bool wide = EPI == EPI_SILU_GATE ? a.N >= 128 : a.N >= 256;
+  if (!tail && wide && a.M > BM && !pair_disabled()) {
+    const int mc = pair_max_clusters<EPI>(num_sms);
+    if (mc > 0) return launch_gemm_pair<EPI>(ta, tb, a, mc, s);
+  }
+  return launch_gemm<256, EPI>(ta, tb, a, num_sms, s);
+}
+
 }  // namespace
 
 size_t gemm_sk_scratch_bytes(int epi, int M, int N, int K, int num_sms) {
@@ -632,15 +910,15 @@ cudaError_t gemm_launch(int epi, const CUtensorMap& ta, const CUtensorMap& tb, c
                         cudaStream_t s) {
   switch (epi) {
     case EPI_STORE:
-      return launch_gemm<256, EPI_STORE>(ta, tb, a, num_sms, s);
+      return launch_gemm_auto<EPI_STORE>(ta, tb, a, num_sms, s);
     case EPI_GATED_RESIDUAL:
-      return launch_gemm<256, EPI_GATED_RESIDUAL>(ta, tb, a, num_sms, s);
+      return launch_gemm_auto<EPI_GATED_RESIDUAL>(ta, tb, a, num_sms, s);
     case EPI_SILU_GATE:
-      return launch_gemm<256, EPI_SILU_GATE>(ta, tb, a, num_sms, s);
+      return launch_gemm_auto<EPI_SILU_GATE>(ta, tb, a, num_sms, s);
     case EPI_STORE_F32:
-      return launch_gemm<256, EPI_STORE_F32>(ta, tb, a, num_sms, s);
+      return launch_gemm_auto<EPI_STORE_F32>(ta, tb, a, num_sms, s);
     case EPI_QKV_ROPE:
-      return launch_gemm<256, EPI_QKV_ROPE>(ta, tb, a, num_sms, s);
+      return launch_gemm_auto<EPI_QKV_ROPE>(ta, tb, a, num_sms, s);
     default:
       return cudaErrorInvalidValue;
   }

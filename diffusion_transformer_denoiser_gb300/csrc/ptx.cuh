@@ -56,28 +56,42 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// CLUSTER: acquire at cluster scope, for phases completed by arrivals from another CTA of the
+// cluster (remote arrives, multicast commits) whose memory effects this thread must then see.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if (CLUSTER) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns false (and the caller
 // must stop its pipeline role) when the CTA was aborted or this wait ran past the limit.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* err, int code, unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  if (mbar_try_wait<CLUSTER>(a, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   uint32_t it = 0;
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(a, parity)) return true;
     if (((++it) & 63u) == 0u) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > limit_ns || it >= kWaitPollCap) {
@@ -91,20 +105,43 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 
 // Warp-uniform wait for roles that go on to warp-collective tcgen05.ld/st: every lane waits, and
 // the warp continues only if every lane saw the phase complete.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                int* err, int code) {
-  const bool ok = mbar_wait(bar, parity, abort_flag, err, code);
+  const bool ok = mbar_wait<CLUSTER>(bar, parity, abort_flag, err, code);
   return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// A wait that ignores the abort flag and gives up only at the wall-clock limit (then it raises
+// the abort flag and records `code`).  For a pair's producers: the leader arms a stage for both
+// CTAs' copies whenever the stage's release (seen by both) arrives, so it never stops early on the
+// abort flag and every copy the follower issues is covered by a phase the leader drains.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_wait_noabort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                                  int code) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait<CLUSTER>(a, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  uint32_t it = 0;
+  while (!mbar_try_wait<CLUSTER>(a, parity)) {
+    if ((++it & 63u) == 0u && (globaltimer_ns() - t0 > kWaitLimitNs || it >= kWaitPollCap)) {
+      *abort_flag = 1;
+      atomicCAS(err, 0, code);
+      return false;
+    }
+  }
+  return true;
 }
 
 // Teardown wait: ignores the abort flag (so copies or MMAs still in flight land before the CTA
 // releases its resources) but still gives up after the wall-clock limit.
+template <bool CLUSTER = false>
 __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, int* err, int code) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return;
+  if (mbar_try_wait<CLUSTER>(a, parity)) return;
   const unsigned long long t0 = globaltimer_ns();
   uint32_t it = 0;
-  while (!mbar_try_wait(a, parity)) {
+  while (!mbar_try_wait<CLUSTER>(a, parity)) {
     if (globaltimer_ns() - t0 > kWaitLimitNs || ++it >= kWaitPollCap) {
       atomicCAS(err, 0, code);
       return;
@@ -231,6 +268,77 @@ __device__ __forceinline__ void tc_commit_warp(uint64_t* bar) {
       "{\n\t.reg .pred e;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+// ------------------------------------------------------------------------------------ CTA pairs
+// A cluster of two CTAs whose tensor cores work as one (tcgen05 cta_group::2): the pair computes a
+// 256-row tile, each CTA holding 128 rows of A, half of the B tile and its own 128 rows of D.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Shared::cluster address of the same shared variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  return a;
+}
+
+// TMA load into this CTA's shared memory whose completion (complete_tx) goes to an mbarrier given by
+// its shared::cluster address, which may be in the other CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m, uint32_t cluster_bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(cluster_bar)
+      : "memory");
+}
+
+// Arrive (release, cluster scope) on an mbarrier in another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D (+)= A * B over the pair, issued by the leader CTA, warp-convergent with an elected lane.
+__device__ __forceinline__ void tc_mma_pair_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier at the same offset in both CTAs of the pair when every tcgen05
+// operation the leader issued so far has completed.
+__device__ __forceinline__ void tc_commit_pair_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
+      ::"r"(smem_u32(bar)), "h"((uint16_t)3)
       : "memory");
 }
 
