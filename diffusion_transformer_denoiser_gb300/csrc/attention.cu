@@ -240,12 +240,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_words = n_kv * 4;
     const bool smem_mask = n_words <= kMaskWords;
     if (smem_mask) {
-      for (int w = warp - 2; w < n_words; w += 8) {
-        const int kc = w * 32 + lane;
-        bool valid = kc < S;
-        if (valid && p.key_mask != nullptr) valid = p.key_mask[(size_t)b * S + kc] != 0;
-        const uint32_t word = __ballot_sync(0xffffffffu, valid);
-        if (lane == 0) mask_words[w] = word;
+      // warp w takes the 128-key chunks w, w + 8, ...; two chunks (8 byte loads per lane, all
+      // independent, so their latencies overlap) per round
+      const uint8_t* km = p.key_mask != nullptr ? p.key_mask + (size_t)b * S : nullptr;
+      for (int c0 = warp - 2; c0 < n_kv; c0 += 16) {
+        uint32_t v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int kc = (c0 + 8 * (i >> 2)) * 128 + (i & 3) * 32 + lane;
+          v[i] = kc < S ? 1u : 0u;
+          if (km != nullptr && kc < S) v[i] = km[kc];
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = c0 + 8 * (i >> 2);
+          const uint32_t word = __ballot_sync(0xffffffffu, v[i] != 0);
+          if (lane == 0 && c < n_kv) mask_words[c * 4 + (i & 3)] = word;
+        }
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");  // the 8 softmax warps only
     }
