@@ -11,7 +11,8 @@
 //   * warp 1   : issues (convergent warp, one elected lane per instruction), per key tile j, in this order
 //                  O0 += P0 V_j,  S0 = Q0 K_{j+1}^T,  O1 += P1 V_j,  S1 = Q1 K_{j+1}^T
 //                so the tensor core works on one query tile while the softmax works on the other.
-//   * warps 2-5 (query tile 0) and 6-9 (query tile 1): one thread per query row.  Scores come
+//   * warps 2-3: idle (they complete the first warpgroup, whose registers go to the softmax).
+//   * warps 4-7 (query tile 0) and 8-11 (query tile 1): one thread per query row.  Scores come
 //                from TMEM; the key tail and masked keys become -inf; the running max lives in
 //                base 2 with log2(e)/sqrt(128) folded into one FMA; P is rounded to bf16 and
 //                written back into TMEM over the scores, where it is the A operand of P V.  O is
@@ -30,7 +31,18 @@ namespace {
 
 constexpr int BQ = 128;
 constexpr int BKV = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+// Register split: the launch gives every thread 168 registers (384 x 168 = 64512 of the SM's
+// 65536).  The first warpgroup (producer, MMA issuer, two idle warps) drops to kRegsControl and
+// the two softmax warpgroups rise to kRegsSoftmax, enough to hold a row's 128 scores with no
+// spill: 128 x 104 + 256 x 200 = 64512, exactly the launch's pool.  The increase waits until
+// the decrease has freed its registers, so the split must fit the pool the kernel was actually
+// launched with; attention_launch checks that before the first launch.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsControl = 104;
+constexpr int kRegsSoftmax = 200;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
+              "register split exceeds the launch pool");
 constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128 x 128 bf16 tile = two 16 KB swizzled halves
 constexpr int HALF_BYTES = TILE_BYTES / 2;
 
@@ -49,8 +61,8 @@ constexpr float kRescaleLog2 = 8.0f;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-// 10 warps put 3 warps on two of the four SM sub-partitions, each with 16K registers: at most 168
-// registers per thread, which the launch bound below lets the compiler derive.
+// 12 warps, 3 per SM sub-partition (16K registers each): 168 registers per thread at launch, which
+// the launch bound below lets the compiler derive; the roles then trade registers as above.
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnArgs p) {
@@ -105,126 +117,132 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------------ TMA producer
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
-      tma_load_3d(sQ, &tmQ, q_full, 0, q0, bh);
-      tma_load_3d(sQ + HALF_BYTES, &tmQ, q_full, 64, q0, bh);
-      tma_load_3d(sQ + TILE_BYTES, &tmQ, q_full, 0, q0 + BQ, bh);
-      tma_load_3d(sQ + TILE_BYTES + HALF_BYTES, &tmQ, q_full, 64, q0 + BQ, bh);
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
+  // The two register regions are separate branches (warpgroup-uniform: every warp of a warpgroup
+  // takes the same one), so the compiler holds each role to its own register budget.
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+    if (warp == 0) {
+      if (lane == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
+        tma_load_3d(sQ, &tmQ, q_full, 0, q0, bh);
+        tma_load_3d(sQ + HALF_BYTES, &tmQ, q_full, 64, q0, bh);
+        tma_load_3d(sQ + TILE_BYTES, &tmQ, q_full, 0, q0 + BQ, bh);
+        tma_load_3d(sQ + TILE_BYTES + HALF_BYTES, &tmQ, q_full, 64, q0 + BQ, bh);
+        int k_issued = 0, v_issued = 0;
+        for (int j = 0; j < n_kv; ++j) {
+          const int st = j & 1;
+          const uint32_t ph = (uint32_t)((j >> 1) & 1);
+          if (!mbar_wait(&k_empty[st], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ATTN + 1)) break;
+          uint8_t* k_dst = sK + st * TILE_BYTES;
+          mbar_arrive_expect_tx(&k_full[st], TILE_BYTES);
+          tma_load_3d(k_dst, &tmK, &k_full[st], 0, j * BKV, bh);
+          tma_load_3d(k_dst + HALF_BYTES, &tmK, &k_full[st], 64, j * BKV, bh);
+          k_issued = j + 1;
+          if (!mbar_wait(&v_empty[st], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ATTN + 1)) break;
+          uint8_t* v_dst = sV + st * TILE_BYTES;
+          mbar_arrive_expect_tx(&v_full[st], TILE_BYTES);
+          tma_load_4d(v_dst, &tmV, &v_full[st], 0, h, j * BKV, b);
+          tma_load_4d(v_dst + HALF_BYTES, &tmV, &v_full[st], 64, h, j * BKV, b);
+          v_issued = j + 1;
+        }
+        // drain the copies still in flight (the last use of each stage)
+        mbar_wait_drain(q_full, 0, p.err, DEV_TIMEOUT_ATTN + 2);
+        for (int j = k_issued - 2 < 0 ? 0 : k_issued - 2; j < k_issued; ++j)
+          mbar_wait_drain(&k_full[j & 1], (j >> 1) & 1, p.err, DEV_TIMEOUT_ATTN + 2);
+        for (int j = v_issued - 2 < 0 ? 0 : v_issued - 2; j < v_issued; ++j)
+          mbar_wait_drain(&v_full[j & 1], (j >> 1) & 1, p.err, DEV_TIMEOUT_ATTN + 2);
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------------ MMA issuer
+      // The whole warp runs this role convergently; each MMA and commit is issued by one elected lane.
+      constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
+      const uint32_t q_addr = smem_u32(sQ);
+      auto issue_s = [&](int i, int j) {  // S_i = Q_i K_j^T
+        const uint32_t qa = q_addr + (uint32_t)i * TILE_BYTES;
+        const uint32_t ka = smem_u32(sK + (j & 1) * TILE_BYTES);
+        const uint32_t d = tmem_base + TM_S + (uint32_t)i * 128u;
+        const uint64_t qd = sdesc_sw128(qa, 16, 1024);
+        const uint64_t kd = sdesc_sw128(ka, 16, 1024);
+  #pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // the start-address field of a descriptor is in 16-byte units
+          const uint32_t off = ((uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u) >> 4;
+          tc_mma_ss_warp(d, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int i, int j) {  // O_i += P_i V_j, P_i from TMEM
+        const uint32_t pa = tmem_base + TM_S + (uint32_t)i * 128u;
+        const uint32_t d = tmem_base + TM_O + (uint32_t)i * 128u;
+        const uint64_t vd = sdesc_sw128(smem_u32(sV + (j & 1) * TILE_BYTES), HALF_BYTES, 1024);
+  #pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // 16 keys per step: 8 packed P columns; V is MN-major (two 8-key groups 1024 B apart,
+          // d halves 16 KB apart)
+          tc_mma_ts_warp(d, pa + (uint32_t)kk * 8u, vd + (uint32_t)kk * (2048u >> 4), idesc_pv,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait_warp(q_full, 0, abort_flag, p.err, DEV_TIMEOUT_ATTN + 3) &&
+                mbar_wait_warp(&k_full[0], 0, abort_flag, p.err, DEV_TIMEOUT_ATTN + 3);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        tc_commit_warp(&s_full[0]);
+        issue_s(1, 0);
+        tc_commit_warp(&s_full[1]);
+        tc_commit_warp(&k_empty[0]);
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
         const int st = j & 1;
         const uint32_t ph = (uint32_t)((j >> 1) & 1);
-        if (!mbar_wait(&k_empty[st], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ATTN + 1)) break;
-        uint8_t* k_dst = sK + st * TILE_BYTES;
-        mbar_arrive_expect_tx(&k_full[st], TILE_BYTES);
-        tma_load_3d(k_dst, &tmK, &k_full[st], 0, j * BKV, bh);
-        tma_load_3d(k_dst + HALF_BYTES, &tmK, &k_full[st], 64, j * BKV, bh);
-        k_issued = j + 1;
-        if (!mbar_wait(&v_empty[st], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ATTN + 1)) break;
-        uint8_t* v_dst = sV + st * TILE_BYTES;
-        mbar_arrive_expect_tx(&v_full[st], TILE_BYTES);
-        tma_load_4d(v_dst, &tmV, &v_full[st], 0, h, j * BKV, b);
-        tma_load_4d(v_dst + HALF_BYTES, &tmV, &v_full[st], 64, h, j * BKV, b);
-        v_issued = j + 1;
-      }
-      // drain the copies still in flight (the last use of each stage)
-      mbar_wait_drain(q_full, 0, p.err, DEV_TIMEOUT_ATTN + 2);
-      for (int j = k_issued - 2 < 0 ? 0 : k_issued - 2; j < k_issued; ++j)
-        mbar_wait_drain(&k_full[j & 1], (j >> 1) & 1, p.err, DEV_TIMEOUT_ATTN + 2);
-      for (int j = v_issued - 2 < 0 ? 0 : v_issued - 2; j < v_issued; ++j)
-        mbar_wait_drain(&v_full[j & 1], (j >> 1) & 1, p.err, DEV_TIMEOUT_ATTN + 2);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    // The whole warp runs this role convergently; each MMA and commit is issued by one elected lane.
-    constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
-    constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
-    const uint32_t q_addr = smem_u32(sQ);
-    auto issue_s = [&](int i, int j) {  // S_i = Q_i K_j^T
-      const uint32_t qa = q_addr + (uint32_t)i * TILE_BYTES;
-      const uint32_t ka = smem_u32(sK + (j & 1) * TILE_BYTES);
-      const uint32_t d = tmem_base + TM_S + (uint32_t)i * 128u;
-      const uint64_t qd = sdesc_sw128(qa, 16, 1024);
-      const uint64_t kd = sdesc_sw128(ka, 16, 1024);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        // the start-address field of a descriptor is in 16-byte units
-        const uint32_t off = ((uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u) >> 4;
-        tc_mma_ss_warp(d, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
-      }
-    };
-    auto issue_pv = [&](int i, int j) {  // O_i += P_i V_j, P_i from TMEM
-      const uint32_t pa = tmem_base + TM_S + (uint32_t)i * 128u;
-      const uint32_t d = tmem_base + TM_O + (uint32_t)i * 128u;
-      const uint64_t vd = sdesc_sw128(smem_u32(sV + (j & 1) * TILE_BYTES), HALF_BYTES, 1024);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        // 16 keys per step: 8 packed P columns; V is MN-major (two 8-key groups 1024 B apart,
-        // d halves 16 KB apart)
-        tc_mma_ts_warp(d, pa + (uint32_t)kk * 8u, vd + (uint32_t)kk * (2048u >> 4), idesc_pv,
-                       (j > 0 || kk > 0) ? 1u : 0u);
-      }
-    };
-    bool ok = mbar_wait_warp(q_full, 0, abort_flag, p.err, DEV_TIMEOUT_ATTN + 3) &&
-              mbar_wait_warp(&k_full[0], 0, abort_flag, p.err, DEV_TIMEOUT_ATTN + 3);
-    if (ok) {
-      tc_fence_after();
-      issue_s(0, 0);
-      tc_commit_warp(&s_full[0]);
-      issue_s(1, 0);
-      tc_commit_warp(&s_full[1]);
-      tc_commit_warp(&k_empty[0]);
-    }
-    for (int j = 0; j < n_kv && ok; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (uint32_t)((j >> 1) & 1);
-      const bool more = j + 1 < n_kv;
-      const int nst = (j + 1) & 1;
-      const uint32_t nph = (uint32_t)(((j + 1) >> 1) & 1);
-      // query tile 0
-      if (!mbar_wait_warp(&p_full[0], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4) ||
-          !mbar_wait_warp(&v_full[st], ph, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      issue_pv(0, j);
-      tc_commit_warp(&o_done[0]);
-      if (more) {
-        if (!mbar_wait_warp(&k_full[nst], nph, abort_flag, p.err, DEV_TIMEOUT_ATTN + 5)) {
+        const bool more = j + 1 < n_kv;
+        const int nst = (j + 1) & 1;
+        const uint32_t nph = (uint32_t)(((j + 1) >> 1) & 1);
+        // query tile 0
+        if (!mbar_wait_warp(&p_full[0], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4) ||
+            !mbar_wait_warp(&v_full[st], ph, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        issue_s(0, j + 1);
-        tc_commit_warp(&s_full[0]);
+        issue_pv(0, j);
+        tc_commit_warp(&o_done[0]);
+        if (more) {
+          if (!mbar_wait_warp(&k_full[nst], nph, abort_flag, p.err, DEV_TIMEOUT_ATTN + 5)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(0, j + 1);
+          tc_commit_warp(&s_full[0]);
+        }
+        // query tile 1
+        if (!mbar_wait_warp(&p_full[1], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 6)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(1, j);
+        tc_commit_warp(&o_done[1]);
+        tc_commit_warp(&v_empty[st]);
+        if (more) {
+          issue_s(1, j + 1);
+          tc_commit_warp(&s_full[1]);
+          tc_commit_warp(&k_empty[nst]);
+        }
       }
-      // query tile 1
-      if (!mbar_wait_warp(&p_full[1], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 6)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      issue_pv(1, j);
-      tc_commit_warp(&o_done[1]);
-      tc_commit_warp(&v_empty[st]);
-      if (more) {
-        issue_s(1, j + 1);
-        tc_commit_warp(&s_full[1]);
-        tc_commit_warp(&k_empty[nst]);
-      }
+      tc_commit_warp(drain);
+      mbar_wait_drain(drain, 0, p.err, DEV_TIMEOUT_ATTN + 7);
     }
-    tc_commit_warp(drain);
-    mbar_wait_drain(drain, 0, p.err, DEV_TIMEOUT_ATTN + 7);
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------------ softmax / epilogue
-    const int wg = (warp - 2) >> 2;  // query tile of this warpgroup
+    const int wg = (warp - 4) >> 2;  // query tile of this warpgroup
     const int qw = warp & 3;         // TMEM lane quarter of this warp
     const int r = qw * 32 + lane;    // query row inside the tile == TMEM lane
     const uint32_t t_lane = tmem_base + ((uint32_t)(qw * 32) << 16);
@@ -243,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // warp w takes the 128-key chunks w, w + 8, ...; two chunks (8 byte loads per lane, all
       // independent, so their latencies overlap) per round
       const uint8_t* km = p.key_mask != nullptr ? p.key_mask + (size_t)b * S : nullptr;
-      for (int c0 = warp - 2; c0 < n_kv; c0 += 16) {
+      for (int c0 = warp - 4; c0 < n_kv; c0 += 16) {
         uint32_t v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -396,6 +414,11 @@ cudaError_t attention_launch(const CUtensorMap& tq, const CUtensorMap& tk, const
   if (!attr_done[dev]) {
     e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
     if (e != cudaSuccess) return e;
+    // the softmax warpgroups' register increase needs the pool the split was sized for
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * kThreads < 128 * kRegsControl + 256 * kRegsSoftmax) return cudaErrorInvalidConfiguration;
     attr_done[dev] = true;
   }
   dim3 grid((a.seq + 2 * BQ - 1) / (2 * BQ), a.n_heads, a.batch);
