@@ -78,10 +78,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = bars + 5;   // [2]
   uint64_t* v_empty = bars + 7;   // [2]
   uint64_t* s_full = bars + 9;    // [2] per query tile
-  uint64_t* p_full = bars + 11;   // [2] per query tile
-  uint64_t* o_done = bars + 13;   // [2] per query tile
-  uint64_t* drain = bars + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* p_full = bars + 11;   // [2][2] per query tile and half of P (keys 0-63, 64-127)
+  uint64_t* o_done = bars + 15;   // [2] per query tile
+  uint64_t* drain = bars + 17;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -101,7 +101,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&p_full[2 * i], 4);
+      mbar_init(&p_full[2 * i + 1], 4);
       mbar_init(&o_done[i], 1);
     }
     mbar_init(drain, 1);
@@ -175,12 +176,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_mma_ss_warp(d, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int i, int j) {  // O_i += P_i V_j, P_i from TMEM
+      auto issue_pv = [&](int i, int j, int half) {  // O_i += P_i V_j over keys [64 half, 64 half + 64)
         const uint32_t pa = tmem_base + TM_S + (uint32_t)i * 128u;
         const uint32_t d = tmem_base + TM_O + (uint32_t)i * 128u;
         const uint64_t vd = sdesc_sw128(smem_u32(sV + (j & 1) * TILE_BYTES), HALF_BYTES, 1024);
   #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 4 * half; kk < 4 * half + 4; ++kk) {
           // 16 keys per step: 8 packed P columns; V is MN-major (two 8-key groups 1024 B apart,
           // d halves 16 KB apart)
           tc_mma_ts_warp(d, pa + (uint32_t)kk * 8u, vd + (uint32_t)kk * (2048u >> 4), idesc_pv,
@@ -203,14 +204,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool more = j + 1 < n_kv;
         const int nst = (j + 1) & 1;
         const uint32_t nph = (uint32_t)(((j + 1) >> 1) & 1);
-        // query tile 0
+        // query tile 0: P V over the first 64 keys as soon as their half of P is in TMEM
         if (!mbar_wait_warp(&p_full[0], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4) ||
             !mbar_wait_warp(&v_full[st], ph, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        issue_pv(0, j);
+        issue_pv(0, j, 0);
+        if (!mbar_wait_warp(&p_full[1], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(0, j, 1);
         tc_commit_warp(&o_done[0]);
         if (more) {
           if (!mbar_wait_warp(&k_full[nst], nph, abort_flag, p.err, DEV_TIMEOUT_ATTN + 5)) {
@@ -222,12 +229,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit_warp(&s_full[0]);
         }
         // query tile 1
-        if (!mbar_wait_warp(&p_full[1], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 6)) {
+        if (!mbar_wait_warp(&p_full[2], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 6)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        issue_pv(1, j);
+        issue_pv(1, j, 0);
+        if (!mbar_wait_warp(&p_full[3], j & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 6)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(1, j, 1);
         tc_commit_warp(&o_done[1]);
         tc_commit_warp(&v_empty[st]);
         if (more) {
@@ -329,24 +342,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = m_cand;
       }
       const float m_use = (m_run == neg_inf()) ? 0.0f : m_run;
-      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      // P in place: word c of sr receives the bf16 pair (2c, 2c+1), whose scores were read at
-      // step c (ascending c never overwrites a score that is still to be read)
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float e0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
-        const float e1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
-        sp[(2 * c) & 7] += e0;
-        sp[(2 * c + 1) & 7] += e1;
-        sr[c] = pack_bf16x2(e0, e1);
-      }
-      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-      l_run = l_run * alpha + sum;
-
       if (j > 0) {
         // O_i holds the P V products up to key tile j-1, all complete: S_i(j), whose completion
         // this warp waited for, was issued after P_i(j-1) V_{j-1} by the same thread, and the
-        // tcgen05 operations of one thread complete in issue order
+        // tcgen05 operations of one thread complete in issue order.  It is rescaled before the
+        // first half of P_i(j) is released to the tensor core.
         if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -359,13 +359,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // P (bf16) over the first 64 columns of S_i
-      tmem_st32(t_s, sr);
-      tmem_st32(t_s + 32, sr + 32);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[wg]);
+      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // P in place, one half of the keys at a time: word c of sr receives the bf16 pair (2c, 2c+1),
+      // whose scores were read at step c (ascending c never overwrites a score still to be read).
+      // Each half goes to TMEM over scores that are already in registers and is released at
+      // once, so P V over keys 0-63 runs while keys 64-127 are exponentiated.
+#pragma unroll
+      for (int hp = 0; hp < 2; ++hp) {
+#pragma unroll
+        for (int c = 32 * hp; c < 32 * hp + 32; ++c) {
+          const float e0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
+          const float e1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
+          sp[(2 * c) & 7] += e0;
+          sp[(2 * c + 1) & 7] += e1;
+          sr[c] = pack_bf16x2(e0, e1);
+        }
+        tmem_st32(t_s + 32 * hp, sr + 32 * hp);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[2 * wg + hp]);
+      }
+      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      l_run = l_run * alpha + sum;
     }
     if (ok && mbar_wait_warp(&o_done[wg], (n_kv - 1) & 1, abort_flag, p.err, DEV_TIMEOUT_ATTN + 10)) {
       tc_fence_after();
