@@ -243,6 +243,27 @@ def test_attention_parity(batch, seq, heads, masked, q_std):
         assert_parity(got[b] if rows is None else got[b][rows], ref, f"attention b={b}")
 
 
+def test_attention_long_sequence_reads_the_mask_per_tile():
+    """Past 65536 keys the key-validity bitmask no longer fits in shared memory and every key tile
+    takes its validity from the mask in global memory: parity on sampled rows, with masked keys
+    on both sides of key 65536 and in the ragged last tile."""
+    mi = require_gpu()
+    batch, seq, heads = 1, 66000, 1
+    rng = np.random.default_rng(66000)
+    qp, kp, qkv = _attn_inputs(rng, batch, seq, heads)
+    mask = np.ones((batch, seq), dtype=np.uint8)
+    mask[:, 3:40] = 0
+    mask[:, 65500:65600] = 0
+    mask[:, 65950:65990] = 0
+    o = torch.empty(batch * seq, heads * 128, dtype=BF, device="cuda")
+    mi.attention(to_dev_bf16(qp), to_dev_bf16(kp), to_dev_bf16(qkv), to_dev(mask), o, batch, seq, heads)
+    torch.cuda.synchronize()
+    assert mi.device_error() == 0
+    got = to_f64(o).reshape(batch, seq, -1)
+    rows = np.unique(np.r_[0:16, 65520:65540, seq - 16:seq, rng.integers(0, seq, 24)])
+    assert_parity(got[0][rows], _attn_ref(qp, kp, qkv, mask, 0, heads, rows), "attention, 66000 keys")
+
+
 def test_attention_equal_scores_cancel():
     # q = 0: every valid key weighs the same; V rows of +-2^10 cancel (the pages' adversarial gate)
     mi = require_gpu()
