@@ -103,6 +103,31 @@ def test_fused_silu_gate_matches_unfused_bytes(m, inter, k):
     assert_parity(to_f64(m2), ref, "gemm+silu gate")
 
 
+def test_gemm_rows_do_not_depend_on_the_launch():
+    """A row's result does not depend on the launch it is computed in: 4130 rows in one launch (CTA
+    pairs, the last 256-row pair tile holding 34 rows) give the bytes of two launches over rows
+    0-4095 (CTA pairs, no ragged tile) and 4096-4129 (34 rows: the one-CTA kernel), and sampled
+    rows on both sides of the boundary match the oracle."""
+    mi = require_gpu()
+    m, inter, k, top_rows = 4130, 8192, 3072, 4096
+    rng = np.random.default_rng(4130)
+    a = to_dev_bf16(_bits(rng, (m, k)))
+    w = to_dev_bf16(_bits(rng, (2 * inter, k), 0.05))
+    full = torch.empty(m, inter, dtype=BF, device="cuda")
+    top = torch.empty(top_rows, inter, dtype=BF, device="cuda")
+    bottom = torch.empty(m - top_rows, inter, dtype=BF, device="cuda")
+    mi.gemm_silu_gate(a, w, full)
+    mi.gemm_silu_gate(a[:top_rows].contiguous(), w, top)
+    mi.gemm_silu_gate(a[top_rows:].contiguous(), w, bottom)
+    torch.cuda.synchronize()
+    assert mi.device_error() == 0
+    assert torch.equal(full[:top_rows].view(torch.int16), top.view(torch.int16))
+    assert torch.equal(full[top_rows:].view(torch.int16), bottom.view(torch.int16))
+    rows = np.r_[0:4, top_rows - 6:top_rows + 6, m - 4:m]
+    ref = O.silu_gate(O.project(to_f64(a)[rows], to_f64(w)), inter)
+    assert_parity(to_f64(full)[rows], ref, "gemm+silu gate, rows across launches")
+
+
 @pytest.mark.parametrize("batch,seq,heads", [(1, 74, 2), (2, 210, 4), (1, 4130, 24)])
 def test_fused_qkv_rope_matches_unfused_bytes(batch, seq, heads):
     mi = require_gpu()
