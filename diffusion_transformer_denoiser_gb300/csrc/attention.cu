@@ -11,6 +11,8 @@
 //   * warp 1   : issues (convergent warp, one elected lane per instruction), per key tile j, in this order
 //                  O0 += P0 V_j,  S0 = Q0 K_{j+1}^T,  O1 += P1 V_j,  S1 = Q1 K_{j+1}^T
 //                so the tensor core works on one query tile while the softmax works on the other.
+//                Each P V is issued in two halves of 64 keys, each as soon as the softmax has
+//                released that half of P.
 //   * warps 2-3: idle (they complete the first warpgroup, whose registers go to the softmax).
 //   * warps 4-7 (query tile 0) and 8-11 (query tile 1): one thread per query row.  Scores come
 //                from TMEM; the key tail and masked keys become -inf; the running max lives in
