@@ -67,65 +67,138 @@ def kernel_bytes(g: mi_synth.Geometry):
 
 
 # ------------------------------------------------------------------------------ clocks
+# Clock-event reason bits of NVML (nvmlClocksEventReason*): the ones a measurement must report.
+NVML_REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
+
+
+def _nvml_index(torch_index: int) -> int:
+    """NVML index of the torch device (CUDA_VISIBLE_DEVICES renumbers the devices torch sees)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v.strip() for v in vis.split(",") if v.strip()]
+    if ids and torch_index < len(ids) and ids[torch_index].isdigit():
+        return int(ids[torch_index])
+    return torch_index
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    """SM clock, power and clock-event reasons sampled every ~2 ms through NVML (read-only queries)
+    on a background thread, so that even a timed region of a few milliseconds holds samples; falls
+    back to nvidia-smi at 200 ms when NVML cannot be loaded."""
 
-    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    SMI_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = None
+    def __init__(self, gpu_index: int, period_s: float = 0.002):
+        self.gpu = _nvml_index(gpu_index)
+        self.period = period_s
+        self.samples = []  # (wall time, sm MHz, max MHz, reason bits, power W)
+        self.source = None
+        self._stop = None
+        self._thread = None
+        self._smi = None
+
+    def _nvml(self):
+        import ctypes
+
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, reasons_fn
 
     def start(self):
-        try:
-            fd, self.path = tempfile.mkstemp(suffix=".csv")
-            os.close(fd)
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
-                                         stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+        import ctypes
+        import threading
 
-    def stop(self, t_begin=None, t_end=None):
-        """Summarise the samples taken between t_begin and t_end (wall clock, seconds)."""
-        if self.proc is None:
-            return None
-        self.proc.terminate()
         try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.fh.close()
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            lib, h, reasons_fn = self._nvml()
+        except (OSError, AttributeError):
+            self._start_smi()
+            return
+        self.source = "nvml"
+        self._stop = threading.Event()
+        mx = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+
+        def run():
+            clk, rs, pw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+            while not self._stop.is_set():
+                ok = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0
+                ok = ok and reasons_fn(h, ctypes.byref(rs)) == 0
+                lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+                if ok:
+                    self.samples.append((time.time(), float(clk.value), float(mx.value), int(rs.value),
+                                         pw.value * 1e-3))
+                time.sleep(self.period)
+
+        self._thread = threading.Thread(target=run, daemon=True)
+        self._thread.start()
+
+    def _start_smi(self):
+        try:
+            fd, self._path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self._fh = open(self._path, "w")
+            self._smi = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.SMI_FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self._fh,
+                                         stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi"
+        except (OSError, FileNotFoundError):
+            self._smi = None
+
+    def _read_smi(self):
         from datetime import datetime
 
-        with open(self.path) as f:
+        self._smi.terminate()
+        try:
+            self._smi.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self._smi.kill()
+        self._fh.close()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self._path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
                 if len(parts) < 10:
                     continue
                 try:
                     ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                    clk = float(parts[2])
-                    mxv = float(parts[3])
+                    clk, mxv = float(parts[2]), float(parts[3])
+                    pw = float(parts[4])
                 except ValueError:
                     continue
-                if t_begin is not None and not (t_begin <= ts <= t_end):
-                    continue
-                sm.append(clk)
-                mx = mxv
+                bits = 0
                 for n, v in zip(names, parts[6:10]):
                     if v.lower() == "active":
-                        reasons.add(n)
-        os.unlink(self.path)
-        if not sm:
+                        bits |= NVML_REASONS[n]
+                self.samples.append((ts, clk, mxv, bits, pw))
+        os.unlink(self._path)
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        elif self._smi is not None:
+            self._read_smi()
+
+    def summary(self, t_begin, t_end):
+        """Median SM clock, max clock, active reasons over the samples taken in [t_begin, t_end]."""
+        sel = [smp for smp in self.samples if t_begin <= smp[0] <= t_end]
+        if not sel:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        bits = 0
+        for smp in sel:
+            bits |= smp[3]
+        return {"sm_mhz": statistics.median(smp[1] for smp in sel), "sm_max_mhz": sel[0][2],
+                "reasons": sorted(n for n, b in NVML_REASONS.items() if bits & b), "samples": len(sel),
+                "power_w_median": statistics.median(smp[4] for smp in sel), "source": self.source,
+                "window_ms": 1e3 * (t_end - t_begin)}
 
 
 # ------------------------------------------------------------------------------ host logic
@@ -168,6 +241,42 @@ def cpu_baseline(g, inp):
     return {"value": n / times[0], "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"one {g.name} block forward for all {n} image-token rows (keys/values from all "
                       f"{g.seq} rows), float64 NumPy, {times[0]:.1f} s"}
+
+
+def oracle_baselines():
+    """The oracle on the host cores at the other configurations (bounded samples, ~30 s in all):
+    the tiny block and the 1200x880 block whole (every image-token row), the long-sequence block on
+    512 sampled image-token query rows (keys and values from all 16418 rows), and one of the 24
+    blocks of the guided step at 1024x1024 (batch 2, both branches, with the embedding and the
+    velocity head), whose time times 24 is reported as the step's, labelled extrapolated."""
+    from oracle import mi_oracle as O
+
+    out = {"cores": os.cpu_count(), "kind": "oracle"}
+    for name in ("tiny_8x8", "block_1200x880"):
+        g = mi_synth.GEOMETRIES[name]
+        inp = mi_synth.block_inputs(g, 0)
+        n, times = oracle_sample_rate(g, inp, g.n_img, 1)
+        out[name] = {"value": n / times[0], "unit": UNIT, "seconds": times[0],
+                     "sample": f"one block forward, all {n} image-token rows"}
+    g = mi_synth.GEOMETRIES["block_2048"]
+    inp = mi_synth.block_inputs(g, 0)
+    n, times = oracle_sample_rate(g, inp, 512, 1)
+    out["block_2048"] = {"value": n / times[0], "unit": UNIT, "seconds": times[0],
+                         "sample": f"{n} of {g.n_img} image-token query rows (keys/values from all {g.seq} rows)"}
+    del inp
+    base = mi_synth.GEOMETRIES["step_1024_cfg"]
+    g1 = mi_synth.Geometry("step_1024_cfg_1block", base.batch, base.text_pad, base.n_text, base.grid_h,
+                           base.grid_w, base.hidden, base.n_heads, base.mlp_inter, n_blocks=1)
+    si = mi_synth.step_inputs(g1, 0)
+    a = O.step_inputs_widened(si)
+    t0 = time.perf_counter()
+    O.denoise_step(**a, dt=-0.02, guidance=3.0)
+    t1 = time.perf_counter() - t0
+    out["step_1024_cfg"] = {"seconds_one_block": t1, "seconds_step_extrapolated": base.n_blocks * t1,
+                            "unit": "s per guided step",
+                            "sample": f"one of {base.n_blocks} blocks of the guided step (batch 2, both branches, "
+                                      "embedding and velocity head), times the block count (extrapolated)"}
+    return out
 
 
 def run_reference(args):
@@ -280,12 +389,14 @@ def run_ours(args):
     if mi.device_error() != 0:
         raise SystemExit("a kernel reported a pipeline timeout during warm-up")
 
-    # ---- timed region: K block forwards back to back
+    # ---- timed region: K block forwards back to back.  The clock sampler polls NVML every ~2 ms
+    # from before the region to the end of the per-kernel timings; each figure keeps the samples
+    # taken inside its own window.
     sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.05)
     barrier()
     torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.5)  # let the sampler come up; only samples inside the timed region count
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     t_begin = time.time()
@@ -296,7 +407,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     t_end = time.time()
     barrier()
-    clocks = sampler.stop(t_begin, t_end)
+    clocks = sampler.summary(t_begin, t_end)
     ms = e0.elapsed_time(e1) / args.steps
     ms_all = [ms]
     if world > 1:
@@ -310,7 +421,8 @@ def run_ours(args):
     err = mi.device_error()
 
     # ---- per-kernel times (same kernels through the single-kernel entry points, same shapes)
-    kern = kernel_times(mi, torch, g, inp, t, devc, stream, reps=max(20, min(200, args.steps)))
+    kern = kernel_times(mi, torch, g, inp, t, devc, reps=max(20, min(200, args.steps)), sampler=sampler)
+    sampler.stop()
 
     # ---- end to end through the public API with host buffers.  Every step copies its input
     # from pinned host memory and its output back to pinned host memory.  Pipelined (the value
@@ -422,6 +534,7 @@ def run_ours(args):
             line["extras"] = extras(mi, torch, devc, stream)
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(g, inp)
+            line["cpu_baseline"]["other_configs"] = oracle_baselines()
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -450,16 +563,9 @@ def _gpu_step_params(torch, g, seed, devc):
                 latent=torch.randn(g.n_img, C, generator=gen, device=devc).to(bf).float())
 
 
-def extras(mi, torch, devc, stream):
-    """The other workloads, timed with CUDA events: the long-sequence block (34 + 128x128 rows), one
-    guided denoising step at 1024x1024 (24 blocks, batch 2: prompt and padded empty negative) and
-    the 50-step Euler loop of that step (guidance 3, t linear in [1, 0]), replayed from a CUDA graph
-    of one step."""
-    out = {}
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    # long-sequence block
-    g = mi_synth.GEOMETRIES["block_2048"]
+def _time_block(mi, torch, devc, name, reps=20):
+    """A block forward of geometry `name` (in place, back to back), timed with CUDA events."""
+    g = mi_synth.GEOMETRIES[name]
     inp = mi_synth.block_inputs(g, 0)
 
     def t(bits):
@@ -472,9 +578,12 @@ def extras(mi, torch, devc, stream):
     args = (t(inp.mod), torch.from_numpy(inp.rope_cos).to(devc), torch.from_numpy(inp.rope_sin).to(devc),
             torch.from_numpy(inp.key_mask).to(devc))
     ws = torch.empty(blk.workspace_size(g.batch, g.seq), dtype=torch.uint8, device=devc)
+    stream = torch.cuda.current_stream()
     for _ in range(3):
         blk.forward(layout, x, x, *args, ws)
-    reps = 20
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(reps):
         blk.forward(layout, x, x, *args, ws)
@@ -482,9 +591,24 @@ def extras(mi, torch, devc, stream):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
     gf, af = flops_of(g)
-    out["block_2048"] = {"ms_per_block": ms, "image_tokens_per_s": g.n_img / (ms * 1e-3),
-                         "tflops": (gf + af) / (ms * 1e-3) / 1e12}
-    del blk, x, ws, args
+    return {"ms_per_block": ms, "image_tokens_per_s": g.batch * g.n_img / (ms * 1e-3),
+            "tflops": (gf + af) / (ms * 1e-3) / 1e12, "rows": g.rows, "forwards": reps}
+
+
+def extras(mi, torch, devc, stream):
+    """The other workloads, timed with CUDA events: the 1200x880 block (63 + 55x75 rows), the
+    long-sequence block (34 + 128x128 rows), one guided denoising step at 1024x1024 (24 blocks,
+    batch 2: prompt and padded empty negative) and the 50-step Euler loop of that step (guidance 3,
+    t linear in [1, 0]), replayed from a CUDA graph of one step."""
+    out = {}
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    peaks, _ = load_peaks()
+    for name in ("block_1200x880", "block_2048"):
+        out[name] = _time_block(mi, torch, devc, name)
+        out[name]["frac_bf16_peak"] = out[name]["tflops"] / peaks["bf16_tflops_sustained"]
+        out[name]["peak"] = "bf16_tflops_sustained (a block is a long mixed step)"
+        torch.cuda.empty_cache()
     # guided step and 50-step loop
     g = mi_synth.GEOMETRIES["step_1024_cfg"]
     prm = _gpu_step_params(torch, g, 7, devc)
@@ -538,112 +662,115 @@ def extras(mi, torch, devc, stream):
     return out
 
 
-def kernel_times(mi, torch, g, inp, t, devc, stream, reps, hbm_sets=8, hbm_rounds=4):
-    """Device time of each kernel of the block, launched alone on the bench stream at the workload's
-    shapes.  Tensor-bound kernels: CUDA events around a CUDA graph of `reps` back-to-back launches
-    (the average).  HBM-bound kernels: a CUDA graph cycling `hbm_rounds` times through `hbm_sets`
-    separate input/output buffer sets (8 x 50.7 MB for the norm, three times the 129 MB L2), so each
-    launch reads inputs that are no longer in L2 and pays for the write-back of earlier outputs."""
+L2_BYTES = 129e6  # GB300 L2
+
+
+def kernel_times(mi, torch, g, inp, t, devc, reps, sampler=None):
+    """Device time of each kernel of the block, launched alone at the workload's shapes through the
+    single-kernel entry points.  Every kernel cycles through enough separate buffer sets (inputs,
+    weights and outputs) that the bytes touched between two uses of one set are at least three
+    times the 129 MB L2: each launch reads its operands from HBM, as the first use inside a forward
+    would, and pays for the write-back of earlier outputs.  Times are CUDA events around one replay
+    of a CUDA graph of those launches, divided by the launch count."""
     R, H, I, nh, S, B = g.rows, g.hidden, g.mlp_inter, g.n_heads, g.seq, g.batch
     bf = torch.bfloat16
     w = inp.weights
-    rng = np.random.default_rng(7)
-
-    def rnd(*shape, std=1.0):
-        return t(mi_synth.bf16_bits(rng.standard_normal(shape) * std))
-
     x = t(inp.x).view(R, H)
     mod = t(inp.mod)
-    h = torch.empty(R, H, dtype=bf, device=devc)
-    qkv = torch.empty(R, 3 * H, dtype=bf, device=devc)
-    qp = torch.empty(B, nh, S, 128, dtype=bf, device=devc)
-    kp = torch.empty_like(qp)
-    o = torch.empty(R, H, dtype=bf, device=devc)
-    x1 = torch.empty(R, H, dtype=bf, device=devc)
-    m = torch.empty(R, I, dtype=bf, device=devc)
-    y = torch.empty(R, H, dtype=bf, device=devc)
     w_qkv, w_o, w_gu, w_d = t(w.w_qkv), t(w.w_o), t(w.w_gu), t(w.w_d)
     wq, wk = t(w.q_norm_w), t(w.k_norm_w)
     cos = torch.from_numpy(inp.rope_cos).to(devc)
     sin = torch.from_numpy(inp.rope_sin).to(devc)
     mask = torch.from_numpy(inp.key_mask).to(devc)
     # realistic operands for each kernel: run the chain once
+    h = torch.empty(R, H, dtype=bf, device=devc)
+    qkv = torch.empty(R, 3 * H, dtype=bf, device=devc)
+    qp = torch.empty(B, nh, S, 128, dtype=bf, device=devc)
+    kp = torch.empty_like(qp)
+    o = torch.empty(R, H, dtype=bf, device=devc)
+    x1 = torch.empty(R, H, dtype=bf, device=devc)
+    h2 = torch.empty(R, H, dtype=bf, device=devc)
+    m = torch.empty(R, I, dtype=bf, device=devc)
     mi.mod_rmsnorm(x, mod, 0, 1, h, B, S, g.eps)
     mi.gemm_qkv_rope(h, w_qkv, wq, wk, cos, sin, qp, kp, qkv, B, S, nh, g.eps)
     mi.attention(qp, kp, qkv, mask, o, B, S, nh)
     mi.gemm_gated_residual(o, w_o, x, mod, 2, x1, S)
-    mi.gemm_silu_gate(h, w_gu, m)
+    mi.mod_rmsnorm(x1, mod, 3, 4, h2, B, S, g.eps)
+    mi.gemm_silu_gate(h2, w_gu, m)
+    torch.cuda.synchronize()
 
-    gemm_f, attn_f = flops_of(g)
-    calls = {
-        "mod_rmsnorm": (lambda: mi.mod_rmsnorm(x, mod, 0, 1, h, B, S, g.eps), {"bytes": 4 * R * H}),
-        "gemm_qkv_rope": (lambda: mi.gemm_qkv_rope(h, w_qkv, wq, wk, cos, sin, qp, kp, qkv, B, S, nh, g.eps),
-                          {"flops": 2.0 * R * 3 * H * H}),
-        "attention": (lambda: mi.attention(qp, kp, qkv, mask, o, B, S, nh), {"flops": float(attn_f)}),
-        "gemm_out_gated_residual": (lambda: mi.gemm_gated_residual(o, w_o, x, mod, 2, x1, S),
-                                    {"flops": 2.0 * R * H * H}),
-        "gemm_gate_up_silu": (lambda: mi.gemm_silu_gate(h, w_gu, m), {"flops": 2.0 * R * 2 * I * H}),
-        "gemm_down_gated_residual": (lambda: mi.gemm_gated_residual(m, w_d, x1, mod, 5, y, S),
-                                     {"flops": 2.0 * R * H * I}),
+    def cl(a):
+        return a.clone()
+
+    def em(a):
+        return torch.empty_like(a)
+
+    _, attn_f = flops_of(g)
+    # name: (buffers of one set, launch on a set, bytes a launch touches, algorithmic work)
+    specs = {
+        "mod_rmsnorm": (lambda: dict(x=cl(x), h=em(h)),
+                        lambda b: mi.mod_rmsnorm(b["x"], mod, 0, 1, b["h"], B, S, g.eps),
+                        4 * R * H, {"bytes": 4 * R * H}),
+        "gemm_qkv_rope": (lambda: dict(h=cl(h), w=cl(w_qkv), qp=em(qp), kp=em(kp), qkv=em(qkv)),
+                          lambda b: mi.gemm_qkv_rope(b["h"], b["w"], wq, wk, cos, sin, b["qp"], b["kp"], b["qkv"],
+                                                     B, S, nh, g.eps),
+                          2 * R * H + 6 * H * H + 6 * R * H, {"flops": 2.0 * R * 3 * H * H}),
+        "attention": (lambda: dict(qp=cl(qp), kp=cl(kp), qkv=cl(qkv), o=em(o)),
+                      lambda b: mi.attention(b["qp"], b["kp"], b["qkv"], mask, b["o"], B, S, nh),
+                      8 * R * H, {"flops": float(attn_f)}),
+        "gemm_out_gated_residual": (lambda: dict(o=cl(o), w=cl(w_o), x=cl(x), y=em(x1)),
+                                    lambda b: mi.gemm_gated_residual(b["o"], b["w"], b["x"], mod, 2, b["y"], S),
+                                    6 * R * H + 2 * H * H, {"flops": 2.0 * R * H * H}),
+        "gemm_gate_up_silu": (lambda: dict(h=cl(h2), w=cl(w_gu), m=em(m)),
+                              lambda b: mi.gemm_silu_gate(b["h"], b["w"], b["m"]),
+                              2 * R * H + 4 * I * H + 2 * R * I, {"flops": 2.0 * R * 2 * I * H}),
+        "gemm_down_gated_residual": (lambda: dict(m=cl(m), w=cl(w_d), x=cl(x1), y=em(x1)),
+                                     lambda b: mi.gemm_gated_residual(b["m"], b["w"], b["x"], mod, 5, b["y"], S),
+                                     2 * R * I + 2 * H * I + 4 * R * H, {"flops": 2.0 * R * H * I}),
     }
     peaks, _ = load_peaks()
-    # rotating buffer sets for the HBM-bound norm
-    xs = [x.clone() for _ in range(hbm_sets)]
-    hs = [torch.empty_like(h) for _ in range(hbm_sets)]
-    hbm_calls = {"mod_rmsnorm": lambda i: mi.mod_rmsnorm(xs[i], mod, 0, 1, hs[i], B, S, g.eps)}
     out = {}
-    for name, (fn, work) in calls.items():
-        for _ in range(3):
-            fn()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    for name, (make, call, touched, work) in specs.items():
+        n_sets = max(2, int(np.ceil(3 * L2_BYTES / touched)))
+        sets = [make() for _ in range(n_sets)]
+        rounds = max(1, int(np.ceil(reps / n_sets)))
+        for b in sets:  # warm-up
+            call(b)
         torch.cuda.synchronize()
-        if "bytes" in work:
-            rot = hbm_calls[name]
-            for i in range(hbm_sets):
-                rot(i)
-            torch.cuda.synchronize()
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph):
-                for _ in range(hbm_rounds):
-                    for i in range(hbm_sets):
-                        rot(i)
-            graph.replay()
-            torch.cuda.synchronize()
-            gstream = torch.cuda.current_stream()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(gstream)
-            graph.replay()
-            e1.record(gstream)
-            torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1) / (hbm_rounds * hbm_sets)
-            del graph
-            gbs = work["bytes"] / (ms * 1e-3) / 1e9
-            out[name] = {"ms": ms, "gbs": gbs, "frac_hbm_peak": gbs / peaks["hbm_gbs"],
-                         "frac_hbm_nominal": gbs / NOMINAL_PEAKS["hbm_gbs"],
-                         "timing": f"average of a CUDA graph cycling {hbm_rounds} times through {hbm_sets} buffer sets "
-                                   f"({hbm_sets * work['bytes'] / 1e6:.0f} MB, more than the 129 MB L2)"}
-            continue
-        # capture the launches in a CUDA graph so host launch overhead does not hide in the timing
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            for _ in range(reps):
-                fn()
+            for _ in range(rounds):
+                for b in sets:
+                    call(b)
         graph.replay()
         torch.cuda.synchronize()
         gstream = torch.cuda.current_stream()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
         e0.record(gstream)
         graph.replay()
         e1.record(gstream)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
-        del graph
+        t1 = time.time()
+        launches = rounds * n_sets
+        ms = e0.elapsed_time(e1) / launches
+        del graph, sets
         ent = {"ms": ms}
-        ent["tflops"] = work["flops"] / (ms * 1e-3) / 1e12
-        ent["frac_bf16_peak"] = ent["tflops"] / peaks["bf16_tflops"]
-        ent["frac_bf16_nominal"] = ent["tflops"] / NOMINAL_PEAKS["bf16_tflops"]
-        ent["timing"] = f"average of a CUDA graph of {reps} back-to-back launches"
+        if "bytes" in work:
+            gbs = work["bytes"] / (ms * 1e-3) / 1e9
+            ent.update(gbs=gbs, frac_hbm_peak=gbs / peaks["hbm_gbs"], frac_hbm_nominal=gbs / NOMINAL_PEAKS["hbm_gbs"])
+        else:
+            tf = work["flops"] / (ms * 1e-3) / 1e12
+            ent.update(tflops=tf, frac_bf16_peak=tf / peaks["bf16_tflops"],
+                       frac_bf16_nominal=tf / NOMINAL_PEAKS["bf16_tflops"])
+        ent["timing"] = (f"average over one CUDA graph of {launches} launches cycling through {n_sets} buffer sets "
+                         f"({n_sets * touched / 1e6:.0f} MB touched per cycle, L2 129 MB)")
+        if sampler is not None:
+            ck = sampler.summary(t0, t1)
+            if ck:
+                ent["sm_mhz"] = ck["sm_mhz"]
+                ent["clock_reasons"] = ck["reasons"]
         out[name] = ent
     return out
 

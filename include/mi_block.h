@@ -107,11 +107,18 @@ typedef struct mi_seq_layout {
 typedef struct mi_block mi_block;
 
 /* Validates the geometry, the weight pointers and the device (sm_103 required, else
- * MI_ERR_UNSUPPORTED) and builds the TMA descriptors of the weights.  Refuses any null weight. */
+ * MI_ERR_UNSUPPORTED) and builds the TMA descriptors of the weights.  Refuses any null weight.
+ * PR #1528, "What it adds": the model's load takes the released geometry only, refuses a tensor
+ * it does not read, and refuses GPUs it was not built for (there sm_120/121, here sm_103).
+ * The weights stay owned by the caller; *out is released with mi_block_destroy. */
 mi_status mi_block_init(mi_block** out, const mi_block_desc* desc);
 void mi_block_destroy(mi_block* blk);
 
-/* Workspace bytes mi_block_forward needs for `batch` elements of `seq` rows. */
+/* Workspace bytes mi_block_forward needs for `batch` elements of `seq` rows: one slab per
+ * intermediate (h, qkv, packed q/k, o, x1, h2, m, plus a and gu/dn when epilogues are not fused)
+ * and the GEMM's stream-K scratch when a projection's plan uses it.  PR #1528, "Measured": the
+ * scratch of a forward is computed from its allocations (0.51 GB there at 1024x1024 with a 34-row
+ * prompt).  Host arithmetic only. */
 mi_status mi_block_workspace_size(const mi_block* blk, int batch, int seq, size_t* bytes);
 
 /* Intermediates left in the workspace by the last forward (for parity checks). */
@@ -135,7 +142,13 @@ mi_status mi_block_tensor_offset(const mi_block* blk, int batch, int seq, int wh
                                  size_t* bytes);
 
 /*
- * One block forward over L->batch elements.
+ * One block forward over L->batch elements: the seven formulas at the top of this file, run as
+ * the page's kernels in its order (PR #1528, "What it adds": modulated RMSNorm, the bf16
+ * projections with fp32 sums, q/k norm and rotary into packed rows, the head-128 attention, the
+ * SiLU gate and the gated adds; its precision bullet: bf16 activations and weights, fp32 sums,
+ * norms and softmax).  Deterministic: PR #1528, "Measured" (the same step run twice gives
+ * identical bytes).  Errors: MI_ERR_INVALID_ARG (layout, pointers), MI_ERR_WORKSPACE (ws too small
+ * or misaligned), MI_ERR_CUDA (a launch failed); nothing is enqueued on an argument error.
  *   x        bf16 [B, S, H] input rows (text rows then image tokens)
  *   y        bf16 [B, S, H] output; y == x (in place) is allowed, any other overlap is not
  *   mod      bf16 [B, 6, H]: shift1, scale1, gate1, shift2, scale2, gate2 for batch element b,
@@ -266,25 +279,32 @@ mi_status mi_time_advance(float* t, int n, float dt, void* stream);
 /* The steps of the block as separate calls (same kernels mi_block_forward launches). */
 
 /* out[r] = x[r] * rsqrt(mean(x[r]^2) + eps) * (1 + mod[b, scale_row]) + mod[b, shift_row],
- * b = r / seq; x, out [batch * seq, hidden]; mod [batch, 6, hidden]. */
+ * b = r / seq; x, out [batch * seq, hidden]; mod [batch, 6, hidden].  PR #1528, "What it adds"
+ * (the modulated RMSNorm kernel; fp32 norm, bf16 out).  out must not overlap x. */
 mi_status mi_mod_rmsnorm(const void* x, const void* mod, int shift_row, int scale_row, void* out, int batch,
                          int seq, int hidden, float eps, void* stream);
 
 /* c[m, n] = sum_k a[m, k] w[n, k] (fp32 sums, bf16 out).  a [m, k], w [n, k], c [m, n];
- * k a multiple of 64, n a multiple of 8. */
+ * k a multiple of 64, n a multiple of 8.  PR #1528, "What it adds" (the projections are bf16 GEMMs
+ * with fp32 sums).  Shapes outside these rules are refused with MI_ERR_UNSUPPORTED. */
 mi_status mi_gemm_bf16(const void* a, const void* w, void* c, int m, int n, int k, void* stream);
 
 /* out = resid + mod[b, gate_row] * bf16(a w^T), b = row / seq (the W_o / W_d projections fused
- * with the gated residual).  resid, out [m, n] (out may equal resid). */
+ * with the gated residual).  resid, out [m, n] (out may equal resid).  PR #1528, "What it adds"
+ * (a bf16 projection with fp32 sums followed by the gated add kernel); same bytes as mi_gemm_bf16
+ * then mi_gated_add. */
 mi_status mi_gemm_bf16_gated_residual(const void* a, const void* w, const void* resid, const void* mod,
                                       int gate_row, void* out, int m, int n, int k, int seq, void* stream);
 
 /* m_out[:, j] = silu(bf16(a wg^T)[:, j]) * bf16(a wu^T)[:, j] with w = [wg; wu] of 2*inter rows
- * (the gate/up projection fused with the SiLU gate).  inter a multiple of 128. */
+ * (the gate/up projection fused with the SiLU gate).  inter a multiple of 128.  PR #1528, "What it
+ * adds" (a bf16 projection, then the SiLU-gate kernel the page lists as "situ"); same bytes as
+ * mi_gemm_bf16 then mi_silu_gate. */
 mi_status mi_gemm_bf16_silu_gate(const void* a, const void* w, void* m_out, int m, int inter, int k,
                                  void* stream);
 
-/* The QKV projection with the q/k RMSNorm + rotary fused into its epilogue: a [batch * seq, H]
+/* PR #1528, "What it adds" (a bf16 projection, then the q/k norm and rotary kernel).
+ * The QKV projection with the q/k RMSNorm + rotary fused into its epilogue: a [batch * seq, H]
  * times w_qkv [3H, H]^T; q and k heads go, normalised and rotated, to qp, kp [batch, heads, seq, 128]
  * (identical bytes to mi_gemm_bf16 followed by mi_qk_norm_rope); the v columns go to columns
  * [2H, 3H) of qkv_v [batch * seq, 3H] (its q/k columns are not written).  H = heads * 128, a multiple
@@ -294,21 +314,28 @@ mi_status mi_gemm_bf16_qkv_rope(const void* a, const void* w_qkv, const void* q_
                                 void* qkv_v, int batch, int seq, int n_heads, float eps, void* stream);
 
 /* Per-head RMSNorm (gains q_norm_w / k_norm_w [128]) and rotary of the q and k columns of
- * qkv [batch * seq, 3H], written to qp, kp [batch, heads, seq, 128]. */
+ * qkv [batch * seq, 3H], written to qp, kp [batch, heads, seq, 128].  PR #1528, "What it adds"
+ * (the kernel for q/k norm and rotary into packed rows).  Rotary pairs are (2p, 2p+1) and use the
+ * table angle at (row, p); the tables are read at base + b * rope_bstride. */
 mi_status mi_qk_norm_rope(const void* qkv, const void* q_norm_w, const void* k_norm_w, const float* rope_cos,
                           const float* rope_sin, int rope_bstride, void* qp, void* kp, int batch, int seq,
                           int n_heads, float eps, void* stream);
 
 /* o [batch * seq, heads * 128] = softmax(q k^T / sqrt(128)) v per (batch, head); q = qp, k = kp
- * as written by mi_qk_norm_rope, v read from columns [2H, 3H) of qkv; key_mask as above. */
+ * as written by mi_qk_norm_rope, v read from columns [2H, 3H) of qkv; key_mask as above.
+ * PR #1528, "What it adds" and "Shared code" (full, non-causal attention at head dim 128; the
+ * softmax in fp32).  qp, kp and qkv must be 16-byte aligned (TMA sources). */
 mi_status mi_attention(const void* qp, const void* kp, const void* qkv, const uint8_t* key_mask, void* o,
                        int batch, int seq, int n_heads, void* stream);
 
-/* out = x + mod[b, gate_row] * y, b = row / seq; x, y, out [batch * seq, hidden]. */
+/* out = x + mod[b, gate_row] * y, b = row / seq; x, y, out [batch * seq, hidden].  PR #1528,
+ * "What it adds" (the gated add kernel; fp32 arithmetic, one bf16 rounding).  out may equal x. */
 mi_status mi_gated_add(const void* x, const void* y, const void* mod, int gate_row, void* out, int batch,
                        int seq, int hidden, void* stream);
 
-/* m[r, j] = silu(gu[r, j]) * gu[r, inter + j]; gu [rows, 2 * inter], m [rows, inter]. */
+/* m[r, j] = silu(gu[r, j]) * gu[r, inter + j]; gu [rows, 2 * inter], m [rows, inter].
+ * silu(z) = z / (1 + exp(-z)).  PR #1528, "What it adds" (the kernel listed as "situ", read as the
+ * SiLU gate); PR #2281, "Three findings" prints the SiLU minimum (-0.278 near -1.278). */
 mi_status mi_silu_gate(const void* gu, void* m, int rows, int inter, void* stream);
 
 #ifdef __cplusplus

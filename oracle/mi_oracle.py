@@ -346,6 +346,26 @@ def step_inputs_widened(si):
                 key_mask=si.key_mask, n_heads=si.geom.n_heads)
 
 
+def step_inputs_widened_lazy(si):
+    """step_inputs_widened, with each block's weights widened only when denoise_step reaches that
+    block (a generator), so a many-block full-size step holds one block in float64 at a time."""
+    a = step_inputs_widened(_StepBlocksDeferred(si))
+    a["blocks"] = (dict(w_qkv=widen(b.w_qkv), w_o=widen(b.w_o), w_gu=widen(b.w_gu), w_d=widen(b.w_d),
+                        q_norm_w=widen(b.q_norm_w), k_norm_w=widen(b.k_norm_w)) for b in si.blocks)
+    return a
+
+
+class _StepBlocksDeferred:
+    """A view of a mi_synth.StepInputs without its blocks (they are widened lazily)."""
+
+    def __init__(self, si):
+        self._si = si
+        self.blocks = []
+
+    def __getattr__(self, name):
+        return getattr(self._si, name)
+
+
 # ----------------------------------------------------------------------------------------------
 # device-side builders (PR #1528 "What it adds": the config, rotary tables and the timestep's
 # modulation are computed by host code shared with the Metal family; here they are computed on

@@ -53,6 +53,10 @@ def assert_parity_combination(got, parts, name=""):
     the same combination of the parts' bounds: sum_k |c_k| * bound_k (triangle inequality).  Guided
     velocities v = v_neg + g (v_pos - v_neg) = (1 - g) v_neg + g v_pos take this bar."""
     ref = sum(c * r for c, r in parts)
+    cos, err, mref = parity_stats(got, ref)
+    plain = cos >= COS_MIN and err <= REL_MAX * mref
+    print(f"{name}: plain bar {'holds' if plain else 'does not hold'} (cosine {cos:.6f}, "
+          f"max|err|/max|ref| {err / mref if mref > 0 else 0.0:.3e})")
     e = np.asarray(got, dtype=np.float64).ravel() - np.asarray(ref, dtype=np.float64).ravel()
     rel_l2 = np.sqrt(2.0 * (1.0 - COS_MIN))
     l2_bound = sum(abs(c) * rel_l2 * np.linalg.norm(r) for c, r in parts)

@@ -1,13 +1,17 @@
 """Full-size geometries: the long-sequence block (34 + 128x128 rows) on sampled rows, the guided step
-at the 1024x1024 geometry (two blocks against the oracle; all 24 blocks for repeatability), and the
-guided step captured in a CUDA graph."""
+at the 1024x1024 geometry (two blocks, and all 24 blocks, against the oracle; all 24 blocks for
+repeatability), and the guided step captured in a CUDA graph."""
+import os
+import time
+
 import numpy as np
 import pytest
 import torch
 
 import mi_synth
 from oracle import mi_oracle as O
-from tests._gpu import assert_parity, assert_parity_combination, require_gpu, to_dev, to_dev_bf16, to_f64
+from tests._gpu import (assert_parity, assert_parity_combination, parity_stats, require_gpu, to_dev, to_dev_bf16,
+                        to_f64)
 
 pytestmark = pytest.mark.gpu
 BF = torch.bfloat16
@@ -54,6 +58,52 @@ def test_step_full_geometry_two_blocks():
     _, vp, vn = _oracle_step(si, 1.0, 3.0)
     assert_parity_combination(to_f64(lat) - O.widen(si.latent), [(-2.0, vn), (3.0, vp)],
                               "guided velocity, 1024x1024 geometry, 2 blocks")
+
+
+@pytest.mark.slow
+def test_step_full_24_blocks_against_oracle():
+    """The whole guided step at full size (24 blocks of the 1024x1024 geometry, batch 2: the prompt's
+    34 rows and the empty negative's 10 rows padded to 34 with a key mask, guidance 3) against the
+    oracle's step on the same seeded bf16 inputs.  Each branch velocity (guidance 1 and 0), the
+    guided velocity and the latent after one step of the default schedule are compared at the
+    per-tensor bar.  The oracle widens one block's weights at a time (24 blocks in float64 would
+    be 21.7 GB) and takes several minutes on the host cores; its time is printed."""
+    mi = require_gpu()
+    from tests.test_gpu_step import GpuStep
+
+    g = mi_synth.GEOMETRIES["step_1024_cfg"]
+    t0 = time.perf_counter()
+    si = mi_synth.step_inputs(g, 0)
+    t_draw = time.perf_counter() - t0
+    gs = GpuStep(mi, si)
+    lat0 = to_dev(mi_synth.bits_to_f32(si.latent))
+    vel = {}
+    for name, guidance in (("guided", 3.0), ("prompt", 1.0), ("negative", 0.0)):
+        lat = lat0.clone()
+        gs.step(lat, 1.0, guidance)  # dt = 1: the latent moves by the velocity
+        vel[name] = to_f64(lat) - O.widen(si.latent)
+    ts = mi_synth.euler_schedule(50)
+    dt = float(ts[1] - ts[0])  # the default schedule's step, -0.02
+    lat = lat0.clone()
+    gs.step(lat, dt, 3.0)
+    lat_new = to_f64(lat)
+    torch.cuda.synchronize()
+    assert mi.device_error() == 0
+    del gs
+
+    a = O.step_inputs_widened_lazy(si)
+    t0 = time.perf_counter()
+    _, vp, vn = O.denoise_step(**a, dt=1.0, guidance=3.0)
+    t_oracle = time.perf_counter() - t0
+    print(f"oracle guided step at full size (24 blocks, batch 2): {t_oracle:.1f} s on {os.cpu_count()} host "
+          f"cores (inputs drawn in {t_draw:.1f} s)")
+    v = O.cfg_combine(vp, vn, 3.0)
+    for name, got, ref in (("prompt velocity", vel["prompt"], vp), ("negative velocity", vel["negative"], vn),
+                           ("guided velocity", vel["guided"], v),
+                           ("latent after one step", lat_new, O.euler_update(O.widen(si.latent), v, dt))):
+        cos, err, mref = parity_stats(got, ref)
+        print(f"{name}: cosine {cos:.6f}, max|err|/max|ref| {err / mref:.3e}")
+        assert_parity(got, ref, f"{name}, full-size guided step")
 
 
 def _gpu_step_weights(g, seed):
