@@ -693,7 +693,9 @@ def kernel_times(mi, torch, g, inp, t, devc, reps, sampler=None):
     m = torch.empty(R, I, dtype=bf, device=devc)
     mi.mod_rmsnorm(x, mod, 0, 1, h, B, S, g.eps)
     mi.gemm_qkv_rope(h, w_qkv, wq, wk, cos, sin, qp, kp, qkv, B, S, nh, g.eps)
-    mi.attention(qp, kp, qkv, mask, o, B, S, nh)
+    # the attention on the schedule the block forward uses (one CTA per SM, split query-tile pairs)
+    attn_ws = torch.empty(mi.attention_workspace_size(B, S, nh), dtype=torch.uint8, device=devc)
+    mi.attention(qp, kp, qkv, mask, o, B, S, nh, ws=attn_ws)
     mi.gemm_gated_residual(o, w_o, x, mod, 2, x1, S)
     mi.mod_rmsnorm(x1, mod, 3, 4, h2, B, S, g.eps)
     mi.gemm_silu_gate(h2, w_gu, m)
@@ -716,7 +718,7 @@ def kernel_times(mi, torch, g, inp, t, devc, reps, sampler=None):
                                                      B, S, nh, g.eps),
                           2 * R * H + 6 * H * H + 6 * R * H, {"flops": 2.0 * R * 3 * H * H}),
         "attention": (lambda: dict(qp=cl(qp), kp=cl(kp), qkv=cl(qkv), o=em(o)),
-                      lambda b: mi.attention(b["qp"], b["kp"], b["qkv"], mask, b["o"], B, S, nh),
+                      lambda b: mi.attention(b["qp"], b["kp"], b["qkv"], mask, b["o"], B, S, nh, ws=attn_ws),
                       8 * R * H, {"flops": float(attn_f)}),
         "gemm_out_gated_residual": (lambda: dict(o=cl(o), w=cl(w_o), x=cl(x), y=em(x1)),
                                     lambda b: mi.gemm_gated_residual(b["o"], b["w"], b["x"], mod, 2, b["y"], S),

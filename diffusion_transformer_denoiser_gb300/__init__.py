@@ -15,7 +15,8 @@ import torch
 
 __all__ = [
     "MiError", "lib", "library_path", "Block", "Model", "SeqLayout", "mod_rmsnorm", "gemm",
-    "gemm_gated_residual", "gemm_silu_gate", "gemm_qkv_rope", "qk_norm_rope", "attention", "gated_add", "silu_gate",
+    "gemm_gated_residual", "gemm_silu_gate", "gemm_qkv_rope", "qk_norm_rope", "attention", "attention_workspace_size",
+    "gated_add", "silu_gate",
     "device_error", "device_supported", "TENSORS", "TimestepModulation", "rope_tables", "time_advance",
 ]
 
@@ -99,6 +100,8 @@ _SIGNATURES = {
     "mi_gemm_bf16_qkv_rope": ([_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P], _I),
     "mi_qk_norm_rope": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _F, _P], _I),
     "mi_attention": ([_P, _P, _P, _P, _P, _I, _I, _I, _P], _I),
+    "mi_attention_workspace_size": ([_I, _I, _I, ctypes.POINTER(_SZ)], _I),
+    "mi_attention_ws": ([_P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P], _I),
     "mi_gated_add": ([_P, _P, _P, _I, _P, _I, _I, _I, _P], _I),
     "mi_silu_gate": ([_P, _P, _I, _I, _P], _I),
 }
@@ -352,9 +355,22 @@ def qk_norm_rope(qkv, q_norm_w, k_norm_w, rope_cos, rope_sin, qp, kp, batch, seq
                                  _ptr(qp, _BF), _ptr(kp, _BF), batch, seq, n_heads, eps, _stream(stream)))
 
 
-def attention(qp, kp, qkv, key_mask, o, batch, seq, n_heads, stream=None):
-    _check(lib().mi_attention(_ptr(qp, _BF), _ptr(kp, _BF), _ptr(qkv, _BF), _ptr(key_mask, torch.uint8),
-                              _ptr(o, _BF), batch, seq, n_heads, _stream(stream)))
+def attention_workspace_size(batch, seq, n_heads) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().mi_attention_workspace_size(batch, seq, n_heads, ctypes.byref(n)))
+    return n.value
+
+
+def attention(qp, kp, qkv, key_mask, o, batch, seq, n_heads, stream=None, ws=None):
+    """Attention; with `ws` (a uint8 tensor of attention_workspace_size bytes) on the split
+    one-CTA-per-SM schedule the block forward uses, without it one CTA per query-tile pair."""
+    if ws is None:
+        _check(lib().mi_attention(_ptr(qp, _BF), _ptr(kp, _BF), _ptr(qkv, _BF), _ptr(key_mask, torch.uint8),
+                                  _ptr(o, _BF), batch, seq, n_heads, _stream(stream)))
+    else:
+        _check(lib().mi_attention_ws(_ptr(qp, _BF), _ptr(kp, _BF), _ptr(qkv, _BF), _ptr(key_mask, torch.uint8),
+                                     _ptr(o, _BF), batch, seq, n_heads, _ptr(ws, torch.uint8) if ws.numel() else None,
+                                     ws.numel(), _stream(stream)))
 
 
 def gated_add(x, y, mod, gate_row, out, batch, seq, stream=None):

@@ -197,6 +197,7 @@ struct WsLayout {
   size_t bytes[11];
   bool present[11];
   size_t sk_off, sk_bytes;  // stream-K scratch of the out and down projections (0 bytes: not used)
+  size_t at_off, at_bytes;  // attention scratch: arrival counters, then the partial results (0: none)
   size_t total;
 };
 
@@ -221,6 +222,9 @@ static WsLayout plan_ws(const mi_block_desc& d, int batch, int seq, int num_sms)
   w.sk_bytes = sk_o > sk_d ? sk_o : sk_d;
   w.sk_off = cur;
   cur = align_up(cur + w.sk_bytes, 1024);
+  w.at_bytes = mi::attention_scratch_bytes(batch, seq, d.n_heads, num_sms);
+  w.at_off = cur;
+  cur = align_up(cur + w.at_bytes, 1024);
   w.total = cur;
   return w;
 }
@@ -278,6 +282,10 @@ static mi_status block_forward_impl(mi_block* blk, int batch, int S, const void*
   bf16* m = mb(base + w.off[MI_T_M]);
   bf16* dn = mb(base + w.off[MI_T_DN]);
   void* sk = w.sk_bytes ? static_cast<void*>(base + w.sk_off) : nullptr;
+  int* at_count = w.at_bytes ? reinterpret_cast<int*>(base + w.at_off) : nullptr;
+  float* at_part = w.at_bytes ? reinterpret_cast<float*>(base + w.at_off + mi::attention_count_bytes(batch, S, nh))
+                              : nullptr;
+  const int at_count_n = w.at_bytes ? (int)(mi::attention_count_bytes(batch, S, nh) / sizeof(int)) : 0;
   const bf16* md = cb(mod);
   const int mbs = 6 * H;  // batch stride of the modulation rows
   cudaError_t e;
@@ -296,8 +304,8 @@ static mi_status block_forward_impl(mi_block* blk, int batch, int S, const void*
     if (!mi::encode_4d_bf16(&tv, qkv + 2 * H, dims, str, box)) return fail(MI_ERR_INVALID_ARG, "tensor map encoding failed (v)");
   }
 
-  // 1. modulated RMSNorm #1
-  e = mi::mod_rmsnorm_launch(cb(x), md + 0 * H, md + 1 * H, mbs, h, R, S, H, d.eps, s);
+  // 1. modulated RMSNorm #1 (it also clears the attention's arrival counters)
+  e = mi::mod_rmsnorm_launch(cb(x), md + 0 * H, md + 1 * H, mbs, h, R, S, H, d.eps, dev->err, s, at_count, at_count_n);
   if (e != cudaSuccess) return cuda_fail(e, "mod_rmsnorm");
   // 2-3. QKV projection; q/k RMSNorm + rotary, packed per head (fused into the projection's epilogue,
   // or a separate kernel when epilogues are not fused)
@@ -334,7 +342,9 @@ static mi_status block_forward_impl(mi_block* blk, int batch, int S, const void*
     aa.out = o;
     aa.scale_log2 = 1.4426950408889634f / sqrtf(128.0f);
     aa.err = dev->err;
-    e = mi::attention_launch(tq, tk, tv, aa, s);
+    aa.part = at_part;
+    aa.count = at_count;
+    e = mi::attention_launch(tq, tk, tv, aa, blk->num_sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   }
   // 5. out projection + gated residual
@@ -357,7 +367,7 @@ static mi_status block_forward_impl(mi_block* blk, int batch, int S, const void*
     if (e != cudaSuccess) return cuda_fail(e, "gated_add");
   }
   // 6. modulated RMSNorm #2
-  e = mi::mod_rmsnorm_launch(x1, md + 3 * H, md + 4 * H, mbs, h2, R, S, H, d.eps, s);
+  e = mi::mod_rmsnorm_launch(x1, md + 3 * H, md + 4 * H, mbs, h2, R, S, H, d.eps, dev->err, s);
   if (e != cudaSuccess) return cuda_fail(e, "mod_rmsnorm");
   // 7. gate/up projection + SiLU gate
   if (d.fuse_epilogues) {
@@ -666,7 +676,7 @@ mi_status mi_denoise_step(mi_model* model, const mi_seq_layout* L, void* latent,
   // velocity head on the image rows, guidance and the Euler update
   const bf16* mf = cb(mod_final);
   e = mi::mod_rmsnorm_rows_launch(x, mf + 0, mf + H, 2 * H, hf, B * N, N, S, L->text_pad, H,
-                                  model->blocks[0]->d.eps, s);
+                                  model->blocks[0]->d.eps, dev->err, s);
   if (e != cudaSuccess) return cuda_fail(e, "final norm");
   {
     CUtensorMap ta;
@@ -694,7 +704,7 @@ mi_status mi_mod_rmsnorm(const void* x, const void* mod, int shift_row, int scal
   if (st != MI_OK) return st;
   const bf16* md = cb(mod);
   cudaError_t e = mi::mod_rmsnorm_launch(cb(x), md + (size_t)shift_row * hidden, md + (size_t)scale_row * hidden,
-                                         6 * hidden, mb(out), batch * seq, seq, hidden, eps,
+                                         6 * hidden, mb(out), batch * seq, seq, hidden, eps, dev->err,
                                          static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MI_OK : cuda_fail(e, "mod_rmsnorm");
 }
@@ -793,8 +803,8 @@ mi_status mi_qk_norm_rope(const void* qkv, const void* q_norm_w, const void* k_n
   return e == cudaSuccess ? MI_OK : cuda_fail(e, "qk_norm_rope");
 }
 
-mi_status mi_attention(const void* qp, const void* kp, const void* qkv, const uint8_t* key_mask, void* o, int batch,
-                       int seq, int n_heads, void* stream) {
+static mi_status attention_common(const void* qp, const void* kp, const void* qkv, const uint8_t* key_mask, void* o,
+                                  int batch, int seq, int n_heads, void* ws, size_t ws_bytes, bool use_ws, void* stream) {
   if (!qp || !kp || !qkv || !o) return fail(MI_ERR_INVALID_ARG, "null tensor argument");
   if (!aligned16(qp) || !aligned16(kp) || !aligned16(qkv) || !aligned16(o))
     return fail(MI_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
@@ -802,6 +812,12 @@ mi_status mi_attention(const void* qp, const void* kp, const void* qkv, const ui
   DeviceInfo* dev = nullptr;
   mi_status st = require_sm103(&dev);
   if (st != MI_OK) return st;
+  const size_t need = use_ws ? mi::attention_scratch_bytes(batch, seq, n_heads, dev->num_sms) : 0;
+  if (need > 0) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+      return fail(MI_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
+    if (ws_bytes < need) return fail(MI_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, need);
+  }
   const int H = n_heads * 128;
   CUtensorMap tq, tk, tv;
   if (!mi::encode_3d_bf16(&tq, qp, 128, (uint64_t)seq, (uint64_t)batch * n_heads, 256, (uint64_t)seq * 256, 64, 128, 1) ||
@@ -819,8 +835,38 @@ mi_status mi_attention(const void* qp, const void* kp, const void* qkv, const ui
   aa.out = mb(o);
   aa.scale_log2 = 1.4426950408889634f / sqrtf(128.0f);
   aa.err = dev->err;
-  cudaError_t e = mi::attention_launch(tq, tk, tv, aa, static_cast<cudaStream_t>(stream));
+  aa.part = nullptr;
+  aa.count = nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (need > 0) {
+    const size_t cb_bytes = mi::attention_count_bytes(batch, seq, n_heads);
+    aa.count = static_cast<int*>(ws);
+    aa.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + cb_bytes);
+    cudaError_t e = cudaMemsetAsync(aa.count, 0, cb_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "attention counters");
+  }
+  cudaError_t e = mi::attention_launch(tq, tk, tv, aa, dev->num_sms, s);
   return e == cudaSuccess ? MI_OK : cuda_fail(e, "attention launch");
+}
+
+mi_status mi_attention(const void* qp, const void* kp, const void* qkv, const uint8_t* key_mask, void* o, int batch,
+                       int seq, int n_heads, void* stream) {
+  return attention_common(qp, kp, qkv, key_mask, o, batch, seq, n_heads, nullptr, 0, false, stream);
+}
+
+mi_status mi_attention_workspace_size(int batch, int seq, int n_heads, size_t* bytes) {
+  if (!bytes) return fail(MI_ERR_INVALID_ARG, "null output pointer");
+  if (batch <= 0 || seq <= 0 || n_heads <= 0) return fail(MI_ERR_INVALID_ARG, "batch, seq, n_heads must be positive");
+  DeviceInfo* dev = nullptr;
+  mi_status st = require_sm103(&dev);
+  if (st != MI_OK) return st;
+  *bytes = mi::attention_scratch_bytes(batch, seq, n_heads, dev->num_sms);
+  return MI_OK;
+}
+
+mi_status mi_attention_ws(const void* qp, const void* kp, const void* qkv, const uint8_t* key_mask, void* o, int batch,
+                          int seq, int n_heads, void* ws, size_t ws_bytes, void* stream) {
+  return attention_common(qp, kp, qkv, key_mask, o, batch, seq, n_heads, ws, ws_bytes, true, stream);
 }
 
 mi_status mi_gated_add(const void* x, const void* y, const void* mod, int gate_row, void* out, int batch, int seq,

@@ -5,6 +5,8 @@
 //
 // All of them move 16-byte vectors (8 bf16) per thread, reduce in fp32 with a fixed shuffle
 // order (so results repeat bit for bit), and round once to bf16 at the output.
+#include <stdlib.h>
+
 #include "mi_internal.h"
 #include "ptx.cuh"
 
@@ -30,36 +32,71 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)
 // out[i] = x[in_row(i)] * rsqrt(mean(x^2) + eps) * (1 + scale[b]) + shift[b]; one warp per row.
 // Row i of the output reads input row (i / out_seq) * in_seq + in_off + i % out_seq, which lets
 // the final norm of a denoising step read only the image rows of each batch element.
-// Persistent warps walk the rows with a stride of the whole grid and load their next row while
-// they finish the current one, so the loads of a row overlap the arithmetic and stores of the last
-// (at the block's 50 MB size this runs at about 86% of a plain copy of the same bytes, against 75%
-// for one row per warp).  NV = hidden / 256, the 16-byte vectors of a row per lane.
-constexpr int kNormMaxVec = 16;  // hidden <= 16 * 256 = 4096
+//
+// Each CTA (one per SM) takes a contiguous range of rows; its warps take every kNormWarps-th row
+// of it.  A warp keeps `depth` of its rows in flight as bulk asynchronous copies into its own
+// shared-memory slots (one mbarrier each), issued before any arithmetic: at the block's 4130 rows
+// every row an SM handles is requested at the start, so the reads stream at full depth from the
+// first microsecond instead of ramping up behind register-held loads.  A row is read from its slot
+// twice (sum of squares, then the outputs, which go straight to global memory) and the slot is then
+// refilled with the warp's row `depth` further on.  The launch is programmatic-dependent: the CTAs start (barrier set-up)
+// while the previous kernel in the stream finishes and wait for its results before the first copy.
+// The arithmetic and its order (per-lane fp32 sums, then a fixed shuffle butterfly) are fixed:
+// results repeat bit for bit.  NV = hidden / 256 (hidden <= 4096).
+constexpr int kNormWarps = 16;
+constexpr int kNormSlotBytes = 192 * 1024;        // shared memory for row slots per CTA
+constexpr int kNormMaxDepth = 4;
 
 template <int NV>
-__global__ void __launch_bounds__(256) mod_rmsnorm_kernel(const __nv_bfloat16* __restrict__ x,
-                                                          const __nv_bfloat16* __restrict__ shift,
-                                                          const __nv_bfloat16* __restrict__ scale, int mod_bstride,
-                                                          __nv_bfloat16* __restrict__ out, int rows, int out_seq,
-                                                          int in_seq, int in_off, int hidden, float eps) {
+__global__ void __launch_bounds__(kNormWarps * 32, 1)
+    mod_rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ shift,
+                       const __nv_bfloat16* __restrict__ scale, int mod_bstride, __nv_bfloat16* __restrict__ out,
+                       int rows, int out_seq, int in_seq, int in_off, int hidden, float eps, int depth, int* err,
+                       int* zero, int zero_n) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  constexpr uint32_t kRowBytes = NV * 512;
+  __shared__ uint64_t bars[kNormWarps * kNormMaxDepth];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_warps = (int)((gridDim.x * blockDim.x) >> 5);
-  int row = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  auto load_row = [&](int r, uint4 (&d)[NV]) {
+  const int r0 = (int)((long long)rows * blockIdx.x / gridDim.x);
+  const int r1 = (int)((long long)rows * (blockIdx.x + 1) / gridDim.x);
+  const int n_mine = (r1 - r0 - warp + kNormWarps - 1) / kNormWarps;  // rows r0 + warp + k * kNormWarps
+  uint64_t* my_bars = bars + warp * kNormMaxDepth;
+  uint8_t* my_slots = smem_raw + (size_t)warp * depth * kRowBytes;
+  if (lane == 0) {
+    for (int i = 0; i < depth; ++i) mbar_init(&my_bars[i], 1);
+    if (warp == 0) abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  grid_dep_wait();  // x may be the previous kernel's output
+  if (zero != nullptr)
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < zero_n; i += gridDim.x * blockDim.x) zero[i] = 0;
+
+  auto issue = [&](int k) {  // lane 0: row k of this warp into slot k % depth
+    const int r = r0 + warp + k * kNormWarps;
     const int in_row = (r / out_seq) * in_seq + in_off + r % out_seq;
-    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)in_row * hidden);
-#pragma unroll
-    for (int i = 0; i < NV; ++i) d[i] = xr[i * 32 + lane];
+    const int sl = k % depth;
+    mbar_arrive_expect_tx(&my_bars[sl], kRowBytes);
+    bulk_load(my_slots + (size_t)sl * kRowBytes, x + (size_t)in_row * hidden, kRowBytes, &my_bars[sl]);
   };
-  uint4 v[NV], nx[NV];
-  if (row < rows) load_row(row, v);
-  for (; row < rows; row += n_warps) {
-    if (row + n_warps < rows) load_row(row + n_warps, nx);
+  int issued = n_mine < depth ? (n_mine > 0 ? n_mine : 0) : depth;
+  if (lane == 0)
+    for (int k = 0; k < issued; ++k) issue(k);
+  grid_dep_launch();
+
+  int k = 0;
+  for (; k < n_mine; ++k) {
+    const int sl = k % depth;
+    if (!mbar_wait_warp(&my_bars[sl], (uint32_t)((k / depth) & 1), &abort_flag, err, DEV_TIMEOUT_NORM + 1)) break;
+    const uint4* src = reinterpret_cast<const uint4*>(my_slots + (size_t)sl * kRowBytes);
+    const int row = r0 + warp + k * kNormWarps;
     float ss = 0.0f;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       float f[8];
-      unpack8(v[i], f);
+      unpack8(src[i * 32 + lane], f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
     }
@@ -71,24 +108,54 @@ __global__ void __launch_bounds__(256) mod_rmsnorm_kernel(const __nv_bfloat16* _
     const uint4* sc = reinterpret_cast<const uint4*>(scale + (size_t)b * mod_bstride);
     uint4* orow = reinterpret_cast<uint4*>(out + (size_t)row * hidden);
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
+    for (int i = 0; i < NV; ++i) {  // the row read again from its slot
       float f[8], fs[8], fc[8];
-      unpack8(v[i], f);
+      unpack8(src[i * 32 + lane], f);
       unpack8(__ldg(sh + i * 32 + lane), fs);
       unpack8(__ldg(sc + i * 32 + lane), fc);
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] = fmaf(f[e] * rstd, 1.0f + fc[e], fs[e]);
       orow[i * 32 + lane] = pack8(f);
     }
-#pragma unroll
-    for (int i = 0; i < NV; ++i) v[i] = nx[i];
+    __syncwarp();  // every lane is done with the slot before it is refilled
+    if (k + depth < n_mine) {
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue(k + depth);
+      }
+      ++issued;
+    }
   }
+  // after an abort: the copies still in flight land before the CTA's shared memory is released
+  if (lane == 0)
+    for (int j = k; j < issued; ++j)
+      mbar_wait_drain(&my_bars[j % depth], (uint32_t)((j / depth) & 1), err, DEV_TIMEOUT_NORM + 2);
 }
 
-// Two CTAs of 8 warps per SM (measured best of 2, 4, 6, 8), never more warps than rows.
+template <int NV>
+cudaError_t mod_rmsnorm_launch_nv(const __nv_bfloat16* x, const __nv_bfloat16* shift, const __nv_bfloat16* scale,
+                                  int mod_bstride, __nv_bfloat16* out, int rows, int out_seq, int in_seq, int in_off,
+                                  int hidden, float eps, int* err, int num_sms, int dev, cudaStream_t s, int* zero,
+                                  int zero_n) {
+  constexpr int kRowBytes = NV * 512;
+  const int depth_fit = kNormSlotBytes / (kNormWarps * kRowBytes);
+  const int depth = depth_fit < kNormMaxDepth ? depth_fit : kNormMaxDepth;
+  const int smem = kNormWarps * depth * kRowBytes;
+  static bool attr_done[kMaxDevices] = {};
+  if (!attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(mod_rmsnorm_kernel<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const int need = (rows + kNormWarps - 1) / kNormWarps;
+  const int grid = need < num_sms ? need : num_sms;
+  return launch_kernel(mod_rmsnorm_kernel<NV>, dim3(grid), dim3(kNormWarps * 32), smem, s, true, x, shift, scale,
+                       mod_bstride, out, rows, out_seq, in_seq, in_off, hidden, eps, depth, err, zero, zero_n);
+}
+
 cudaError_t mod_rmsnorm_any(const __nv_bfloat16* x, const __nv_bfloat16* shift, const __nv_bfloat16* scale,
                             int mod_bstride, __nv_bfloat16* out, int rows, int out_seq, int in_seq, int in_off,
-                            int hidden, float eps, cudaStream_t s) {
+                            int hidden, float eps, int* err, cudaStream_t s, int* zero, int zero_n) {
   static int sms_cache[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -98,15 +165,12 @@ cudaError_t mod_rmsnorm_any(const __nv_bfloat16* x, const __nv_bfloat16* shift, 
     e = cudaDeviceGetAttribute(&sms_cache[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
   }
-  const int want = 2 * sms_cache[dev];
-  const int need = (rows + 7) / 8;
-  const int blocks = need < want ? need : want;
+  if (rows <= 0) return cudaSuccess;
   switch (hidden >> 8) {
-#define MI_NORM_CASE(n)                                                                                           \
-  case n:                                                                                                         \
-    mod_rmsnorm_kernel<n><<<blocks, 256, 0, s>>>(x, shift, scale, mod_bstride, out, rows, out_seq, in_seq, in_off, \
-                                                 hidden, eps);                                                    \
-    break;
+#define MI_NORM_CASE(n)                                                                                          \
+  case n:                                                                                                        \
+    return mod_rmsnorm_launch_nv<n>(x, shift, scale, mod_bstride, out, rows, out_seq, in_seq, in_off, hidden, eps, \
+                                    err, sms_cache[dev], dev, s, zero, zero_n);
     MI_NORM_CASE(1) MI_NORM_CASE(2) MI_NORM_CASE(3) MI_NORM_CASE(4) MI_NORM_CASE(5) MI_NORM_CASE(6) MI_NORM_CASE(7)
     MI_NORM_CASE(8) MI_NORM_CASE(9) MI_NORM_CASE(10) MI_NORM_CASE(11) MI_NORM_CASE(12) MI_NORM_CASE(13)
     MI_NORM_CASE(14) MI_NORM_CASE(15) MI_NORM_CASE(16)
@@ -114,7 +178,6 @@ cudaError_t mod_rmsnorm_any(const __nv_bfloat16* x, const __nv_bfloat16* shift, 
     default:
       return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------------------------ q/k pack
@@ -334,18 +397,25 @@ int grid_for(long long work_items, int threads) {
 
 }  // namespace
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("MI_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
 cudaError_t mod_rmsnorm_launch(const __nv_bfloat16* x, const __nv_bfloat16* shift, const __nv_bfloat16* scale,
-                               int mod_bstride, __nv_bfloat16* out, int rows, int seq, int hidden, float eps,
-                               cudaStream_t s) {
-  if (rows <= 0) return cudaSuccess;
-  return mod_rmsnorm_any(x, shift, scale, mod_bstride, out, rows, seq, seq, 0, hidden, eps, s);
+                               int mod_bstride, __nv_bfloat16* out, int rows, int seq, int hidden, float eps, int* err,
+                               cudaStream_t s, int* zero, int zero_n) {
+  return mod_rmsnorm_any(x, shift, scale, mod_bstride, out, rows, seq, seq, 0, hidden, eps, err, s, zero, zero_n);
 }
 
 cudaError_t mod_rmsnorm_rows_launch(const __nv_bfloat16* x, const __nv_bfloat16* shift, const __nv_bfloat16* scale,
                                     int mod_bstride, __nv_bfloat16* out, int rows, int out_seq, int in_seq, int in_off,
-                                    int hidden, float eps, cudaStream_t s) {
-  if (rows <= 0) return cudaSuccess;
-  return mod_rmsnorm_any(x, shift, scale, mod_bstride, out, rows, out_seq, in_seq, in_off, hidden, eps, s);
+                                    int hidden, float eps, int* err, cudaStream_t s) {
+  return mod_rmsnorm_any(x, shift, scale, mod_bstride, out, rows, out_seq, in_seq, in_off, hidden, eps, err, s,
+                         nullptr, 0);
 }
 
 cudaError_t qk_norm_rope_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* wq, const __nv_bfloat16* wk,

@@ -323,6 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dep_wait();  // the operands may be the previous kernel's outputs
+  grid_dep_launch();
 
   const int num_m = (p.M + BM - 1) / BM;
   const int num_n = (EPI == EPI_SILU_GATE) ? (p.N / (BN / 2)) : (p.N + BN - 1) / BN;
@@ -629,6 +631,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // both CTAs' barriers exist before any remote arrive or multicast commit
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dep_wait();  // the operands may be the previous kernel's outputs
+  grid_dep_launch();
 
   const int num_pm = (p.M + 2 * BM - 1) / (2 * BM);
   const int num_n = (EPI == EPI_SILU_GATE) ? (p.N / (BN / 2)) : (p.N + BN - 1) / BN;
@@ -830,8 +834,8 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
       if (e != cudaSuccess) return e;
     }
   }
-  kern<<<grid, kThreads, L::TOTAL, s>>>(ta, tb, a);
-  return cudaGetLastError();
+  // no programmatic launch after the counters' memset: it is not a kernel the launch could overlap
+  return launch_kernel(kern, dim3(grid), dim3(kThreads), L::TOTAL, s, a.sk_tiles == 0, ta, tb, a);
 }
 
 // MI_GEMM_PAIRS=0 keeps every GEMM on the one-CTA kernel (for comparisons).
@@ -877,8 +881,8 @@ cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const
   const int num_n = (EPI == EPI_SILU_GATE) ? (a.N / 128) : (a.N + 255) / 256;
   const int units = num_pm * num_n;
   const int clusters = units < max_clusters ? units : max_clusters;
-  gemm_pair_kernel<EPI><<<2 * clusters, kThreads, PairSmem::TOTAL, s>>>(ta, tb, a);
-  return cudaGetLastError();
+  return launch_kernel(gemm_pair_kernel<EPI>, dim3(2 * clusters), dim3(kThreads), PairSmem::TOTAL, s, true, ta, tb,
+                       a);
 }
 
 // The pair kernel serves launches of more than one 128-row block and at least one full column tile

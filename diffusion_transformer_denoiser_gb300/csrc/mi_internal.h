@@ -62,16 +62,28 @@ struct AttnArgs {
   __nv_bfloat16* out;          // [B, S, n_heads * 128]
   float scale_log2;            // log2(e) / sqrt(128)
   int* err;
+  // Scratch of attention_scratch_bytes() (256-byte aligned) or null.  With it the grid is one CTA
+  // per SM and units may be split between neighbouring CTAs; without it, one CTA per unit.
+  float* part;                 // partial results of split units, two slots per CTA
+  int* count;                  // [units][2] arrival counters, zero at launch (left zero after it)
 };
 
 // q/k maps: 3-D over (128, S, B * n_heads); v map: 4-D over (128, n_heads, S, B) of the qkv buffer.
 cudaError_t attention_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                             const AttnArgs& a, cudaStream_t s);
+                             const AttnArgs& a, int num_sms, cudaStream_t s);
+// CTAs of a launch (num_sms <= 0: one per unit, no splits).
+int attention_grid(int batch, int seq, int n_heads, int num_sms);
+// Scratch bytes of the split schedule (0 when there are no more units than SMs), and the bytes of
+// its arrival counters, which come first.
+size_t attention_scratch_bytes(int batch, int seq, int n_heads, int num_sms);
+size_t attention_count_bytes(int batch, int seq, int n_heads);
 
 // Element-wise kernels (elementwise.cu).
+// zero/zero_n: an int array the kernel clears (after the previous kernel in the stream is done),
+// for counters a later kernel of the same forward needs at zero; null for none.
 cudaError_t mod_rmsnorm_launch(const __nv_bfloat16* x, const __nv_bfloat16* shift, const __nv_bfloat16* scale,
                                int mod_bstride, __nv_bfloat16* out, int rows, int seq, int hidden, float eps,
-                               cudaStream_t s);
+                               int* err, cudaStream_t s, int* zero = nullptr, int zero_n = 0);
 cudaError_t qk_norm_rope_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* wq, const __nv_bfloat16* wk,
                                 const float* cos, const float* sin, int rope_bstride, __nv_bfloat16* qp,
                                 __nv_bfloat16* kp, int batch, int seq, int n_heads, float eps, cudaStream_t s);
@@ -82,7 +94,7 @@ cudaError_t assemble_seq_launch(const __nv_bfloat16* text, const __nv_bfloat16* 
                                 int text_pad, int n_img, int hidden, cudaStream_t s);
 cudaError_t mod_rmsnorm_rows_launch(const __nv_bfloat16* x, const __nv_bfloat16* shift, const __nv_bfloat16* scale,
                                     int mod_bstride, __nv_bfloat16* out, int rows, int out_seq, int in_seq, int in_off,
-                                    int hidden, float eps, cudaStream_t s);
+                                    int hidden, float eps, int* err, cudaStream_t s);
 cudaError_t copy_rows_launch(const __nv_bfloat16* src, __nv_bfloat16* dst, size_t n_elems, cudaStream_t s);
 cudaError_t cfg_euler_launch(const float* vel, float* latent, int n_img, int channels, float dt, float guidance,
                              int batch, cudaStream_t s);
@@ -94,6 +106,27 @@ cudaError_t silu_inplace_launch(__nv_bfloat16* v, long long n, cudaStream_t s);
 cudaError_t modulation_split_launch(const __nv_bfloat16* all, __nv_bfloat16* mods, __nv_bfloat16* fin, int batch,
                                     int n_blocks, int hidden, cudaStream_t s);
 cudaError_t time_advance_launch(float* t, int n, float dt, cudaStream_t s);
+
+// Programmatic dependent launch (PDL): a kernel launched with it may start its prologue while the
+// previous kernel in the stream is still running; it waits in griddepcontrol.wait before its first
+// global-memory access.  On unless the environment sets MI_PDL=0 (read once per process).
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                          Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (pdl && pdl_enabled()) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // Self-test of the bounded pipeline waits (selftest.cu).
 cudaError_t wait_timeout_selftest_launch(int* err, unsigned long long limit_ns, cudaStream_t s);

@@ -19,6 +19,7 @@ enum : int {
   DEV_TIMEOUT_ATTN = 0x200,
   DEV_TIMEOUT_SELFTEST = 0x300,
   DEV_SCHEDULE_GEMM = 0x400,  // a GEMM launch whose stream-K plan the kernel cannot carry out
+  DEV_TIMEOUT_NORM = 0x500,
 };
 
 // Wall-clock limit of a single wait (ns).  No legitimate wait in these kernels lasts more than a
@@ -177,6 +178,20 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       "r"(smem_u32(bar))
       : "memory");
 }
+
+// Non-tensor bulk copy of `bytes` (a multiple of 16) from global to shared memory, both addresses
+// 16-byte aligned; its completion is counted (complete_tx) on the mbarrier `bar` of this CTA.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Programmatic dependent launch: wait until the grids this launch depends on have completed and
+// their memory is visible (a no-op for a launch without the programmatic attribute), and allow
+// the next launch in the stream to begin its own prologue.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (UMMA, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -65,11 +65,13 @@ mi_status mi_device_error(int* code);
 
 /* Error codes mi_device_error reports: 0x100 + k (a GEMM wait), 0x200 + k (an attention wait),
  * 0x300 (the self-test below), 0x400 (a GEMM whose split of tail tiles over the CTAs has more parts
- * per tile than its fix-up adds; the library's own plans never produce one). */
+ * per tile than its fix-up adds; the library's own plans never produce one), 0x500 + k (a wait of
+ * the modulated RMSNorm for its row copies). */
 #define MI_DEV_TIMEOUT_GEMM 0x100
 #define MI_DEV_TIMEOUT_ATTN 0x200
 #define MI_DEV_TIMEOUT_SELFTEST 0x300
 #define MI_DEV_SCHEDULE_GEMM 0x400
+#define MI_DEV_TIMEOUT_NORM 0x500
 
 /* Enqueues a one-CTA kernel whose pipeline wait can never complete: the wait gives up after
  * limit_us microseconds (at most 1e6), records MI_DEV_TIMEOUT_SELFTEST in the device error flag and
@@ -327,6 +329,16 @@ mi_status mi_qk_norm_rope(const void* qkv, const void* q_norm_w, const void* k_n
  * softmax in fp32).  qp, kp and qkv must be 16-byte aligned (TMA sources). */
 mi_status mi_attention(const void* qp, const void* kp, const void* qkv, const uint8_t* key_mask, void* o,
                        int batch, int seq, int n_heads, void* stream);
+
+/* mi_attention on the schedule mi_block_forward uses: one CTA per SM, each taking an equal share of
+ * the (query-tile pair, key tile) steps, so no SM idles in a partial last wave.  A pair of query
+ * tiles whose keys are split between two CTAs is finished by the second to arrive, which adds the
+ * two partial results (unnormalised output, running max and sum) in a fixed order, so results
+ * repeat bit for bit.  ws: at least mi_attention_workspace_size bytes, 256-byte aligned (0 bytes,
+ * and ws may be NULL, when there are no more query-tile pairs than SMs).  Same page as above. */
+mi_status mi_attention_workspace_size(int batch, int seq, int n_heads, size_t* bytes);
+mi_status mi_attention_ws(const void* qp, const void* kp, const void* qkv, const uint8_t* key_mask, void* o,
+                          int batch, int seq, int n_heads, void* ws, size_t ws_bytes, void* stream);
 
 /* out = x + mod[b, gate_row] * y, b = row / seq; x, y, out [batch * seq, hidden].  PR #1528,
  * "What it adds" (the gated add kernel; fp32 arithmetic, one bf16 rounding).  out may equal x. */

@@ -244,10 +244,21 @@ def _attn_ref(qp, kp, qkv, mask, b, heads, rows=None):
     return O.attention(q, k, v, valid).reshape(q.shape[0], H)
 
 
+def _attn_ws(mi, batch, seq, heads, split):
+    """The split schedule's workspace (None: one CTA per query-tile pair)."""
+    if not split:
+        return None
+    return torch.empty(mi.attention_workspace_size(batch, seq, heads), dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("split", [False, True], ids=["unit_per_cta", "split_per_sm"])
 @pytest.mark.parametrize("batch,seq,heads,masked,q_std", [
     (1, 74, 2, False, 1.0), (1, 336, 4, False, 1.0), (2, 210, 4, True, 1.0), (1, 300, 2, False, 4.0),
-    (1, 128, 2, False, 1.0), (1, 1, 2, False, 1.0), (1, 4130, 24, False, 1.0), (1, 4188, 24, True, 1.0)])
-def test_attention_parity(batch, seq, heads, masked, q_std):
+    (1, 128, 2, False, 1.0), (1, 1, 2, False, 1.0), (1, 4130, 24, False, 1.0), (1, 4188, 24, True, 1.0),
+    (2, 1000, 40, True, 1.0)])
+def test_attention_parity(batch, seq, heads, masked, q_std, split):
+    # (2, 1000, 40): 320 query-tile pairs on the split schedule, whose CTA boundaries fall inside
+    # pairs of both batch elements (the key mask is rebuilt when a CTA moves to the second)
     mi = require_gpu()
     rng = np.random.default_rng(seq * 13 + heads)
     qp, kp, qkv = _attn_inputs(rng, batch, seq, heads, q_std)
@@ -258,7 +269,7 @@ def test_attention_parity(batch, seq, heads, masked, q_std):
         mask[-1, 100:140] = 0
     o = torch.empty(batch * seq, heads * 128, dtype=BF, device="cuda")
     mi.attention(to_dev_bf16(qp), to_dev_bf16(kp), to_dev_bf16(qkv), None if mask is None else to_dev(mask), o,
-                 batch, seq, heads)
+                 batch, seq, heads, ws=_attn_ws(mi, batch, seq, heads, split))
     torch.cuda.synchronize()
     assert mi.device_error() == 0
     got = to_f64(o).reshape(batch, seq, -1)
@@ -266,6 +277,40 @@ def test_attention_parity(batch, seq, heads, masked, q_std):
         rows = None if seq <= 1024 else np.unique(np.r_[0:40, seq - 40:seq, rng.integers(0, seq, 100)])
         ref = _attn_ref(qp, kp, qkv, mask, b, heads, rows)
         assert_parity(got[b] if rows is None else got[b][rows], ref, f"attention b={b}")
+
+
+def test_attention_split_parts_repeat_and_agree():
+    """The split schedule at the 1024x1024 block's shape (408 query-tile pairs on one CTA per SM):
+    repeats bit for bit, agrees with the one-CTA-per-pair schedule within the bar (the two add
+    partial sums in different places), and a key mask covering the first half of the keys leaves
+    some split parts with no valid key at all (their weight in the combination is zero)."""
+    mi = require_gpu()
+    rng = np.random.default_rng(77)
+    batch, seq, heads = 1, 4130, 24
+    qp, kp, qkv = (to_dev_bf16(a) for a in _attn_inputs(rng, batch, seq, heads))
+    ws = _attn_ws(mi, batch, seq, heads, True)
+    assert ws.numel() > 0
+    outs = []
+    for masked in (False, True):
+        mask = np.ones((batch, seq), dtype=np.uint8)
+        if masked:
+            mask[:, :2048] = 0
+        m = to_dev(mask)
+        o1 = torch.empty(batch * seq, heads * 128, dtype=BF, device="cuda")
+        o2 = torch.empty_like(o1)
+        o3 = torch.empty_like(o1)
+        mi.attention(qp, kp, qkv, m, o1, batch, seq, heads, ws=ws)
+        mi.attention(qp, kp, qkv, m, o2, batch, seq, heads, ws=ws)
+        mi.attention(qp, kp, qkv, m, o3, batch, seq, heads)
+        torch.cuda.synchronize()
+        assert mi.device_error() == 0
+        assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+        assert_parity(to_f64(o1), to_f64(o3), f"split against unsplit schedule, masked={masked}")
+        outs.append((mask, o1))
+    mask, o = outs[1]
+    rows = np.unique(np.r_[0:20, seq - 20:seq, rng.integers(0, seq, 60)])
+    ref = _attn_ref(*(bf16_to_bits(t) for t in (qp, kp, qkv)), mask, 0, heads, rows)
+    assert_parity(to_f64(o)[rows], ref, "split schedule, first half of the keys masked")
 
 
 def test_attention_long_sequence_reads_the_mask_per_tile():
@@ -280,13 +325,15 @@ def test_attention_long_sequence_reads_the_mask_per_tile():
     mask[:, 3:40] = 0
     mask[:, 65500:65600] = 0
     mask[:, 65950:65990] = 0
-    o = torch.empty(batch * seq, heads * 128, dtype=BF, device="cuda")
-    mi.attention(to_dev_bf16(qp), to_dev_bf16(kp), to_dev_bf16(qkv), to_dev(mask), o, batch, seq, heads)
-    torch.cuda.synchronize()
-    assert mi.device_error() == 0
-    got = to_f64(o).reshape(batch, seq, -1)
-    rows = np.unique(np.r_[0:16, 65520:65540, seq - 16:seq, rng.integers(0, seq, 24)])
-    assert_parity(got[0][rows], _attn_ref(qp, kp, qkv, mask, 0, heads, rows), "attention, 66000 keys")
+    for split in (False, True):  # 258 query-tile pairs: the split schedule cuts pairs of 516 key tiles
+        o = torch.empty(batch * seq, heads * 128, dtype=BF, device="cuda")
+        mi.attention(to_dev_bf16(qp), to_dev_bf16(kp), to_dev_bf16(qkv), to_dev(mask), o, batch, seq, heads,
+                     ws=_attn_ws(mi, batch, seq, heads, split))
+        torch.cuda.synchronize()
+        assert mi.device_error() == 0
+        got = to_f64(o).reshape(batch, seq, -1)
+        rows = np.unique(np.r_[0:16, 65520:65540, seq - 16:seq, rng.integers(0, seq, 24)])
+        assert_parity(got[0][rows], _attn_ref(qp, kp, qkv, mask, 0, heads, rows), f"attention, 66000 keys, split={split}")
 
 
 def test_attention_equal_scores_cancel():
@@ -334,15 +381,18 @@ def test_attention_masked_keys_carry_nothing():
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
 
 
-def test_attention_all_keys_masked_gives_zero():
+@pytest.mark.parametrize("batch,seq,heads", [(2, 150, 2), (2, 700, 48)], ids=["unit_per_cta", "split_per_sm"])
+def test_attention_all_keys_masked_gives_zero(batch, seq, heads):
+    # (2, 700, 48): 288 query-tile pairs on the split schedule; the pairs of the masked element
+    # that are split have two parts with no valid key
     mi = require_gpu()
-    batch, seq, heads = 2, 150, 2
     rng = np.random.default_rng(23)
     qp, kp, qkv = _attn_inputs(rng, batch, seq, heads)
     mask = np.ones((batch, seq), dtype=np.uint8)
     mask[1, :] = 0
     o = torch.empty(batch * seq, heads * 128, dtype=BF, device="cuda")
-    mi.attention(to_dev_bf16(qp), to_dev_bf16(kp), to_dev_bf16(qkv), to_dev(mask), o, batch, seq, heads)
+    mi.attention(to_dev_bf16(qp), to_dev_bf16(kp), to_dev_bf16(qkv), to_dev(mask), o, batch, seq, heads,
+                 ws=_attn_ws(mi, batch, seq, heads, heads > 2))
     got = to_f64(o).reshape(batch, seq, -1)
     assert np.all(got[1] == 0.0)
     assert_parity(got[0], _attn_ref(qp, kp, qkv, mask, 0, heads), "attention b=0")

@@ -5,6 +5,7 @@ with different inputs (the static array keeps the previous call's contents), and
 float64 oracle.  This file sorts last so that a run stopping at the first failure has already
 run every other test."""
 import ctypes
+import dataclasses
 
 import numpy as np
 import pytest
@@ -82,7 +83,8 @@ def test_static_workspace_forward_matches_caller_workspace(geom):
         # the same kernels on the same inputs: the same bytes
         assert torch.equal(y_static.view(torch.int16), y_ref.view(torch.int16)), \
             f"static-workspace forward differs from the caller-workspace forward (seed {seed})"
-        ref = O.block_forward_inputs(inp)["y"]
+        # the block holds the first call's weights; the second call changes activations and modulation
+        ref = O.block_forward_inputs(dataclasses.replace(inp, weights=w))["y"]
         assert_parity(to_f64(y_static), ref, f"static-workspace forward against the oracle, seed {seed}")
 
 
