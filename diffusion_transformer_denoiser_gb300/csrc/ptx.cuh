@@ -105,10 +105,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // Warp-uniform wait for roles that go on to warp-collective tcgen05.ld/st: every lane waits, and
-// the warp continues only if every lane saw the phase complete.
+// the warp continues only if every lane saw the phase complete.  Fast path: when the first test
+// finds the phase complete in all 32 lanes at once (the mask of lanes executing that branch is
+// full, so no lane saw it incomplete), the warp continues without a vote; otherwise every lane goes
+// through the bounded wait and the vote.  A vote costs the issuing warps of the attention and the
+// GEMMs a noticeable share of their issue slots while they share an SM sub-partition with busy warps.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                int* err, int code) {
+  if (mbar_try_wait<CLUSTER>(smem_u32(bar), parity) && __activemask() == 0xffffffffu) return true;
   const bool ok = mbar_wait<CLUSTER>(bar, parity, abort_flag, err, code);
   return __all_sync(0xffffffffu, ok) != 0;
 }
