@@ -2,28 +2,40 @@
 //
 // The pages run the block's attention through a templated head-128 attention kernel with fp32
 // softmax (MOSS-Image transformer on CUDA, "What it adds" and "Shared code").  This kernel is
-// written for the 5th-generation tensor cores.  One CTA owns two 128-row query tiles of one
-// (batch, head) and streams the keys once for both:
-//   * warp 0   : TMA producer: both Q tiles once, then K and V tiles of 128 keys into a 2-stage
-//                ring (K and V with their own barriers so a K slot frees as soon as both score
-//                products have read it).  K comes from the packed [B, heads, S, 128] rows; V is
-//                read in place from the QKV projection output through a strided 4-D map.
+// written for the 5th-generation tensor cores.  The unit of work is a pair of 128-row query tiles
+// of one (batch, head); the keys are streamed once for both tiles.  The grid is persistent: one
+// CTA per SM takes an equal share of all (unit, key tile) steps, a contiguous range cut into
+// segments of one unit each, so no SM idles in a partial last wave.  A unit cut between two CTAs
+// is finished by whichever part arrives second: the first writes its unnormalised O, running max
+// and sum to scratch, the second adds both parts in a fixed order (keys from 0 first) and stores.
+// Without scratch (or with more units than fit the list), the grid is one CTA per unit.
+//   * warp 0   : TMA producer: the Q tiles of each segment, then K and V tiles of 128 keys into a
+//                2-stage ring (K and V with their own barriers so a K slot frees as soon as both
+//                score products have read it).  K comes from the packed [B, heads, S, 128] rows; V
+//                is read in place from the QKV projection output through a strided 4-D map.
 //   * warp 1   : issues (convergent warp, one elected lane per instruction), per key tile j, in this order
 //                  O0 += P0 V_j,  S0 = Q0 K_{j+1}^T,  O1 += P1 V_j,  S1 = Q1 K_{j+1}^T
 //                so the tensor core works on one query tile while the softmax works on the other.
 //                Each P V is issued in two halves of 64 keys, each as soon as the softmax has
-//                released that half of P.
-//   * warps 2-3: idle (they complete the first warpgroup, whose registers go to the softmax).
+//                released that half of P.  A warp's MMA issue stalls while the tensor core's queue
+//                is full and the issuer shares its SM sub-partition with two softmax warps, so its
+//                loop carries nothing it can leave to others:
+//   * warp 2   : wait proxy: waits for V of each key tile and K of the next and adds an arrival to
+//                query tile 0's P barriers, which therefore imply those copies for the issuer.
+//   * warp 3   : idle (it completes the first warpgroup, whose registers go to the softmax).
 //   * warps 4-7 (query tile 0) and 8-11 (query tile 1): one thread per query row.  Scores come
 //                from TMEM; the key tail and masked keys become -inf; the running max lives in
-//                base 2 with log2(e)/sqrt(128) folded into one FMA; P is rounded to bf16 and
-//                written back into TMEM over the scores, where it is the A operand of P V.  O is
-//                rescaled in TMEM only when a row's max grows by more than 2^8 (the stale max
-//                keeps every exponent <= 2^8, so P stays exact enough in bf16 and the sum in fp32).
+//                base 2 with log2(e)/sqrt(128) folded into one FMA (packed f32x2, as the row sum);
+//                P is rounded to bf16 and written back into TMEM over the scores, where it is the A
+//                operand of P V.  O is rescaled in TMEM only when a row's max grows by more than
+//                2^8 (the stale max keeps every exponent <= 2^8, so P stays exact enough in bf16 and
+//                the sum in fp32).  At a segment's end they normalise and store O (or write or
+//                combine the parts of a cut unit) and release O for the next segment.
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); P_i = first 64
 // columns of S_i.  tcgen05.mma operations of one thread execute in issue order, so S_i(j+1) may be
 // issued right after the P_i(j) V_j product that still reads P_i(j) from the same columns.  Tile
-// order and reduction order are fixed: results repeat bit for bit.
+// order, segment boundaries (a function of the shape and the SM count) and reduction order are
+// fixed: results repeat bit for bit.
 #include "mi_internal.h"
 #include "ptx.cuh"
 
@@ -132,8 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[2 * i], 4);
-      mbar_init(&p_full[2 * i + 1], 4);
+      // query tile 0's halves also count the wait proxy's arrival (V of the key tile, K of the next)
+      mbar_init(&p_full[2 * i], i == 0 ? 5 : 4);
+      mbar_init(&p_full[2 * i + 1], i == 0 ? 5 : 4);
       mbar_init(&o_done[i], 1);
       mbar_init(&o_empty[i], 4);
     }
@@ -211,6 +224,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = v_issued - 2 < 0 ? 0 : v_issued - 2; j < v_issued; ++j)
           mbar_wait_drain(&v_full[j & 1], (uint32_t)((j >> 1) & 1), p.err, DEV_TIMEOUT_ATTN + 2);
       }
+    } else if (warp == 2) {
+      // ------------------------------------------------------------------ wait proxy
+      // Waits for V of each key tile and for K of the next one and adds an arrival to the matching
+      // half of query tile 0's P barrier, so that the MMA issuer (whose every instruction sits on
+      // the chain) needs no wait of its own for them: through these release/acquire pairs its wait
+      // for P also orders the copies before its products.
+      const int n_seg = *seg_count;
+      int kt = 0;
+      bool ok = true;
+      for (int seg = 0; ok && seg < n_seg; ++seg) {
+        const int n = seg_tab[seg].z - seg_tab[seg].y;
+        for (int t = 0; t < n; ++t, ++kt) {
+          // each arrival belongs to the phase of key tile kt: the previous phase of the barrier
+          // must be complete first (the copies often land a key tile ahead of the softmax)
+          const uint32_t prev = (uint32_t)((kt - 1) & 1);
+          if ((kt > 0 && !mbar_wait_warp(&p_full[0], prev, abort_flag, p.err, DEV_TIMEOUT_ATTN + 9)) ||
+              !mbar_wait_warp(&v_full[kt & 1], (uint32_t)((kt >> 1) & 1), abort_flag, p.err, DEV_TIMEOUT_ATTN + 9)) {
+            ok = false;
+            break;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_full[0]);
+          if ((kt > 0 && !mbar_wait_warp(&p_full[1], prev, abort_flag, p.err, DEV_TIMEOUT_ATTN + 9)) ||
+              (t + 1 < n &&
+               !mbar_wait_warp(&k_full[(kt + 1) & 1], (uint32_t)(((kt + 1) >> 1) & 1), abort_flag, p.err,
+                               DEV_TIMEOUT_ATTN + 9))) {
+            ok = false;
+            break;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_full[1]);
+        }
+      }
     } else if (warp == 1) {
       // ------------------------------------------------------------------ MMA issuer
       // The whole warp runs this role convergently; each MMA and commit is issued by one elected lane.
@@ -268,11 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < n; ++t) {
           kt = kt0 + t;
           const int st = (kt & 1);
-          const uint32_t ph = (uint32_t)((kt >> 1) & 1);
           const uint32_t pp = (uint32_t)(kt & 1);
           const bool more = t + 1 < n;
           const int nst = ((kt + 1) & 1);
-          const uint32_t nph = (uint32_t)(((kt + 1) >> 1) & 1);
           const bool first = t == 0;
           // at a segment's first key tile, the previous segment's O has been read out
           if (first && seg > 0 &&
@@ -282,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           // query tile 0: P V over the first 64 keys as soon as their half of P is in TMEM
-          if (!mbar_wait_warp(&p_full[0], pp, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4) ||
-              !mbar_wait_warp(&v_full[st], ph, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4)) {
+          // (the first half of P_0 also implies that V of this key tile has landed: the wait proxy)
+          if (!mbar_wait_warp(&p_full[0], pp, abort_flag, p.err, DEV_TIMEOUT_ATTN + 4)) {
             ok = false;
             break;
           }
@@ -296,11 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_pv(0, st, 1, first);
           tc_commit_warp(&o_done[0]);
-          if (more) {
-            if (!mbar_wait_warp(&k_full[nst], nph, abort_flag, p.err, DEV_TIMEOUT_ATTN + 5)) {
-              ok = false;
-              break;
-            }
+          if (more) {  // the second half of P_0 implies that K of the next key tile has landed
             tc_fence_after();
             issue_s(0, nst);
             tc_commit_warp(&s_full[0]);
