@@ -28,6 +28,12 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
+__device__ __forceinline__ f32x2_t f2_mul(f32x2_t a, f32x2_t b) {
+  f32x2_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // ------------------------------------------------------------------------------------ adaLN norm
 // out[i] = x[in_row(i)] * rsqrt(mean(x^2) + eps) * (1 + scale[b]) + shift[b]; one warp per row.
 // Row i of the output reads input row (i / out_seq) * in_seq + in_off + i % out_seq, which lets
@@ -41,8 +47,8 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)
 // twice (sum of squares, then the outputs, which go straight to global memory) and the slot is then
 // refilled with the warp's row `depth` further on.  The launch is programmatic-dependent: the CTAs start (barrier set-up)
 // while the previous kernel in the stream finishes and wait for its results before the first copy.
-// The arithmetic and its order (per-lane fp32 sums, then a fixed shuffle butterfly) are fixed:
-// results repeat bit for bit.  NV = hidden / 256 (hidden <= 4096).
+// The arithmetic and its order (per-lane fp32 sums on two packed lanes, then a fixed shuffle
+// butterfly) are fixed: results repeat bit for bit.  NV = hidden / 256 (hidden <= 4096).
 constexpr int kNormWarps = 16;
 constexpr int kNormSlotBytes = 192 * 1024;        // shared memory for row slots per CTA
 constexpr int kNormMaxDepth = 4;
@@ -92,14 +98,21 @@ __global__ void __launch_bounds__(kNormWarps * 32, 1)
     if (!mbar_wait_warp(&my_bars[sl], (uint32_t)((k / depth) & 1), &abort_flag, err, DEV_TIMEOUT_NORM + 1)) break;
     const uint4* src = reinterpret_cast<const uint4*>(my_slots + (size_t)sl * kRowBytes);
     const int row = r0 + warp + k * kNormWarps;
-    float ss = 0.0f;
+    // sum of squares on packed pairs (f32x2): half the FMA instructions of a per-element chain
+    f32x2_t ss2 = 0ull;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
-      float f[8];
-      unpack8(src[i * 32 + lane], f);
+      const uint4 v = src[i * 32 + lane];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+      for (int e = 0; e < 4; ++e) {
+        const f32x2_t f = f2_pack(bf16_lo(w[e]), bf16_hi(w[e]));
+        ss2 = f2_fma(f, f, ss2);
+      }
     }
+    float ss_lo, ss_hi;
+    f2_unpack(ss2, ss_lo, ss_hi);
+    float ss = ss_lo + ss_hi;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float rstd = rsqrtf(ss / (float)hidden + eps);
@@ -107,15 +120,24 @@ __global__ void __launch_bounds__(kNormWarps * 32, 1)
     const uint4* sh = reinterpret_cast<const uint4*>(shift + (size_t)b * mod_bstride);
     const uint4* sc = reinterpret_cast<const uint4*>(scale + (size_t)b * mod_bstride);
     uint4* orow = reinterpret_cast<uint4*>(out + (size_t)row * hidden);
+    const f32x2_t rstd2 = f2_pack(rstd, rstd);
+    const f32x2_t one2 = f2_pack(1.0f, 1.0f);
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {  // the row read again from its slot
-      float f[8], fs[8], fc[8];
-      unpack8(src[i * 32 + lane], f);
-      unpack8(__ldg(sh + i * 32 + lane), fs);
-      unpack8(__ldg(sc + i * 32 + lane), fc);
+    for (int i = 0; i < NV; ++i) {  // the row read again from its slot; (x * rstd) * (1 + scale) + shift
+      const uint4 v = src[i * 32 + lane];
+      const uint4 vs = __ldg(sh + i * 32 + lane);
+      const uint4 vc = __ldg(sc + i * 32 + lane);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w}, ws[4] = {vs.x, vs.y, vs.z, vs.w}, wc[4] = {vc.x, vc.y, vc.z, vc.w};
+      uint32_t o[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = fmaf(f[e] * rstd, 1.0f + fc[e], fs[e]);
-      orow[i * 32 + lane] = pack8(f);
+      for (int e = 0; e < 4; ++e) {
+        const f32x2_t t = f2_mul(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), rstd2);
+        const f32x2_t c = f2_add(f2_pack(bf16_lo(wc[e]), bf16_hi(wc[e])), one2);
+        float lo, hi;
+        f2_unpack(f2_fma(t, c, f2_pack(bf16_lo(ws[e]), bf16_hi(ws[e]))), lo, hi);
+        o[e] = pack_bf16x2(lo, hi);
+      }
+      orow[i * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
     }
     __syncwarp();  // every lane is done with the slot before it is refilled
     if (k + depth < n_mine) {
