@@ -885,16 +885,33 @@ cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const
                        a);
 }
 
-// The pair kernel serves launches of more than one 128-row block and at least one full column tile
-// that do not take the stream-K tail; the one-CTA kernel keeps the others (a single row block, the
-// narrow velocity projection, long-k tail launches).
+// Launches the pair kernel may serve: more than one 128-row block and at least one full column tile.
+bool pair_shape(int epi, int M, int N) {
+  const bool wide = epi == EPI_SILU_GATE ? N >= 128 : N >= 256;
+  return wide && M > BM && !pair_disabled();
+}
+
+// Whether a launch (given stream-K scratch) runs on the one-CTA kernel with a stream-K tail: the
+// few-tile long-k launches (fewer of its tiles than SMs, whose k-blocks it spreads over up to twice
+// as many CTAs) and tail launches the pair kernel cannot serve.  A launch with at least a wave of
+// one-CTA tiles goes to the pair kernel instead, on its plain schedule: at 8260 x 3072 x 8192 (the
+// guided step's down projection) and 16418 rows the pair kernel beats the one-CTA stream-K tail.
+bool one_cta_tail(int epi, int M, int N, int K, int num_sms) {
+  if (!(epi == EPI_STORE || epi == EPI_GATED_RESIDUAL || epi == EPI_STORE_F32)) return false;
+  int g = 0;
+  if (sk_plan(M, N, K, num_sms, 256, &g) == 0) return false;
+  const int tiles = ((M + BM - 1) / BM) * ((N + 255) / 256);
+  return tiles < num_sms || !pair_shape(epi, M, N);
+}
+
+// The pair kernel serves the launches of pair_shape() that do not take the one-CTA stream-K tail;
+// the one-CTA kernel keeps the others (a single row block, the narrow velocity projection, the
+// few-tile long-k launches).
 template <int EPI>
 cudaError_t launch_gemm_auto(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int num_sms,
                              cudaStream_t s) {
-  int g = 0;
-  const bool tail = kStreamK<EPI> && a.sk_scratch != nullptr && sk_plan(a.M, a.N, a.K, num_sms, 256, &g) > 0;
-  const bool wide = EPI == EPI_SILU_GATE ? a.N >= 128 : a.N >= 256;
-  if (!tail && wide && a.M > BM && !pair_disabled()) {
+  const bool tail = a.sk_scratch != nullptr && one_cta_tail(EPI, a.M, a.N, a.K, num_sms);
+  if (!tail && pair_shape(EPI, a.M, a.N)) {
     const int mc = pair_max_clusters<EPI>(num_sms);
     if (mc > 0) return launch_gemm_pair<EPI>(ta, tb, a, mc, s);
   }
@@ -904,9 +921,7 @@ cudaError_t launch_gemm_auto(const CUtensorMap& ta, const CUtensorMap& tb, const
 }  // namespace
 
 size_t gemm_sk_scratch_bytes(int epi, int M, int N, int K, int num_sms) {
-  if (!(epi == EPI_STORE || epi == EPI_GATED_RESIDUAL || epi == EPI_STORE_F32)) return 0;
-  int g = 0;
-  if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0 || sk_plan(M, N, K, num_sms, 256, &g) == 0) return 0;
+  if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0 || !one_cta_tail(epi, M, N, K, num_sms)) return 0;
   return sk_count_bytes(num_sms) + (size_t)2 * num_sms * BM * 256 * sizeof(float);
 }
 

@@ -79,8 +79,10 @@ GEOMETRIES: Dict[str, Geometry] = {
     "block_1024": Geometry("block_1024", 1, 34, (34,), 64, 64, 3072, 24, 8192),
     # single block at 1200x880 (75 wide x 55 high grid), 63 text rows: ragged tiles
     "block_1200x880": Geometry("block_1200x880", 1, 63, (63,), 55, 75, 3072, 24, 8192),
-    # the guided step's block on its own (batch 2: prompt 34 rows, negative 10 rows padded to 34);
-    # its down projection runs the GEMM's stream-K tail
+    # small batch-2 layout with a deep MLP (I = 8448): its down projection has 4 row tiles of
+    # 132 k-blocks, fewer tiles than SMs, which the GEMM spreads along k (its stream-K tail)
+    "small_cfg_b2_streamk": Geometry("small_cfg_b2_streamk", 2, 18, (18, 5), 12, 16, 256, 2, 8448),
+    # the guided step's block on its own (batch 2: prompt 34 rows, negative 10 rows padded to 34)
     "block_1024_cfg_b2": Geometry("block_1024_cfg_b2", 2, 34, (34, 10), 64, 64, 3072, 24, 8192),
     # long sequence: 128x128 grid (about 2048x2048 picture) + 34 text rows
     "block_2048": Geometry("block_2048", 1, 34, (34,), 128, 128, 3072, 24, 8192),

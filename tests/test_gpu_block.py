@@ -100,12 +100,14 @@ def test_block_parity_full_size(name):
     _check_all(gb, oracle_block(name), True)
 
 
-def test_fused_and_unfused_give_identical_bytes_on_the_stream_k_tail():
-    # at this geometry (8260 rows) the down projection splits its last full wave and remainder of
-    # tiles along k over all SMs in both paths; the partial sums are added in a fixed order, so the
-    # two paths still agree exactly, and so do repeats
+@pytest.mark.parametrize("name", ["small_cfg_b2_streamk", "block_1024_cfg_b2"])
+def test_fused_and_unfused_give_identical_bytes_at_batch_2(name):
+    # small_cfg_b2_streamk: the down projection (4 row tiles, 132 k-blocks) spreads its k-blocks
+    # over twice as many CTAs in both paths (the stream-K tail), and the partial sums are added in a
+    # fixed order; block_1024_cfg_b2: the guided step's block (8260 rows), every projection on the
+    # CTA-pair kernel.  Either way the two paths agree exactly, and so do repeats.
     mi = require_gpu()
-    inp = mi_synth.block_inputs(mi_synth.GEOMETRIES["block_1024_cfg_b2"], 3)
+    inp = mi_synth.block_inputs(mi_synth.GEOMETRIES[name], 3)
     a = GpuBlock(mi, inp, True)
     b = GpuBlock(mi, inp, False)
     ya = a.run().clone()

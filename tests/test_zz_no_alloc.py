@@ -24,7 +24,7 @@ STATIC_WS_BYTES = 64 << 20
 # 128-row block) takes the GEMM's stream-K tail: its k-blocks are split over two CTAs per tile,
 # whose fp32 partial sums and arrival counters live in the workspace.  The counters must start at
 # zero on every call, which is what a second call through the shared static array checks.
-STREAM_K_GEOM = mi_synth.Geometry("small_cfg_b2_streamk", 2, 18, (18, 5), 12, 16, 256, 2, 8448)
+STREAM_K_GEOM = mi_synth.GEOMETRIES["small_cfg_b2_streamk"]
 
 
 def _ptr(t):
