@@ -1,8 +1,9 @@
 // Inline-PTX helpers for sm_103a: mbarriers, TMA bulk-tensor loads, tcgen05 (UMMA + TMEM).
 //
-// Every spin-wait in this library goes through mbar_wait(), which gives up after a wall-clock
-// limit, records an error code in a device-global flag and raises a CTA-local abort flag so the
-// other warps of the CTA stop waiting too.  A kernel that aborted still releases its TMEM.
+// Every spin-wait in this library goes through mbar_wait() or its two variants below, which give up
+// after a bounded number of polls, record an error code in a device-global flag and raise a
+// CTA-local abort flag so the other warps of the CTA stop waiting too.  A kernel that aborted still
+// releases its TMEM.
 #pragma once
 
 #include <cuda.h>
@@ -22,12 +23,13 @@ enum : int {
   DEV_TIMEOUT_NORM = 0x500,
 };
 
-// Wall-clock limit of a single wait (ns).  No legitimate wait in these kernels lasts more than a
-// few milliseconds; the limit only turns a pipeline bug into an error status instead of a hang.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
-// Backstop on the number of polls of one wait (seconds of polling at any realistic poll rate), so a
-// wait ends even if the global timer were not advancing.
-constexpr uint32_t kWaitPollCap = 1u << 28;
+// Polls of a single wait.  A poll (mbarrier.try_wait) that finds the phase incomplete suspends the
+// thread for about 1.48 us on GB300 (measured) before it returns, so the bound is about 1.5 s.  No
+// legitimate wait in these kernels lasts more than a few milliseconds; the bound only turns a
+// pipeline bug into an error status instead of a hang.  A poll count, not a clock, keeps the slow
+// path of each of the many inlined waits short: the kernels' speed depends on the size of their
+// code (instruction-cache misses), and a thread that is not running does not use up its polls.
+constexpr uint32_t kWaitPolls = 1u << 20;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -83,25 +85,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns false (and the caller
-// must stop its pipeline role) when the CTA was aborted or this wait ran past the limit.
+// must stop its pipeline role) when the CTA was aborted or this wait ran out of polls.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err, int code, unsigned long long limit_ns = kWaitLimitNs) {
+                                          int* err, int code, uint32_t max_polls = kWaitPolls) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait<CLUSTER>(a, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  uint32_t it = 0;
-  while (true) {
+#pragma unroll 1
+  for (uint32_t it = 0; it < max_polls; ++it) {
     if (mbar_try_wait<CLUSTER>(a, parity)) return true;
-    if (((++it) & 63u) == 0u) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit_ns || it >= kWaitPollCap) {
-        *abort_flag = 1;
-        atomicCAS(err, 0, code);
-        return false;
-      }
-    }
+    if ((it & 63u) == 63u && *abort_flag) return false;
   }
+  *abort_flag = 1;
+  atomicCAS(err, 0, code);
+  return false;
 }
 
 // Warp-uniform wait for roles that go on to warp-collective tcgen05.ld/st: every lane waits, and
@@ -118,41 +114,31 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-// A wait that ignores the abort flag and gives up only at the wall-clock limit (then it raises
-// the abort flag and records `code`).  For a pair's producers: the leader arms a stage for both
-// CTAs' copies whenever the stage's release (seen by both) arrives, so it never stops early on the
-// abort flag and every copy the follower issues is covered by a phase the leader drains.
+// A wait that ignores the abort flag and gives up only when its polls run out (then it raises the
+// abort flag and records `code`).  For a pair's producers: the leader arms a stage for both CTAs'
+// copies whenever the stage's release (seen by both) arrives, so it never stops early on the abort
+// flag and every copy the follower issues is covered by a phase the leader drains.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_noabort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
                                                   int code) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait<CLUSTER>(a, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  uint32_t it = 0;
-  while (!mbar_try_wait<CLUSTER>(a, parity)) {
-    if ((++it & 63u) == 0u && (globaltimer_ns() - t0 > kWaitLimitNs || it >= kWaitPollCap)) {
-      *abort_flag = 1;
-      atomicCAS(err, 0, code);
-      return false;
-    }
-  }
-  return true;
+#pragma unroll 1
+  for (uint32_t it = 0; it < kWaitPolls; ++it)
+    if (mbar_try_wait<CLUSTER>(a, parity)) return true;
+  *abort_flag = 1;
+  atomicCAS(err, 0, code);
+  return false;
 }
 
 // Teardown wait: ignores the abort flag (so copies or MMAs still in flight land before the CTA
-// releases its resources) but still gives up after the wall-clock limit.
+// releases its resources) but still gives up when its polls run out.
 template <bool CLUSTER = false>
 __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, int* err, int code) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait<CLUSTER>(a, parity)) return;
-  const unsigned long long t0 = globaltimer_ns();
-  uint32_t it = 0;
-  while (!mbar_try_wait<CLUSTER>(a, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs || ++it >= kWaitPollCap) {
-      atomicCAS(err, 0, code);
-      return;
-    }
-  }
+#pragma unroll 1
+  for (uint32_t it = 0; it < kWaitPolls; ++it)
+    if (mbar_try_wait<CLUSTER>(a, parity)) return;
+  atomicCAS(err, 0, code);
 }
 
 // ------------------------------------------------------------------------------------ TMA

@@ -59,7 +59,7 @@ mi_status mi_device_supported(void);
 
 /* Reads and clears the device error flag of the current device.  *code = 0 when every kernel
  * since the last call finished its pipeline; otherwise the first timeout code recorded (a kernel
- * whose wait exceeded its wall-clock limit returns early and leaves its outputs undefined).
+ * whose wait ran out of polls, about 1.5 s, returns early and leaves its outputs undefined).
  * Synchronises the device (diagnostic call, not for the hot path). */
 mi_status mi_device_error(int* code);
 
@@ -73,9 +73,10 @@ mi_status mi_device_error(int* code);
 #define MI_DEV_SCHEDULE_GEMM 0x400
 #define MI_DEV_TIMEOUT_NORM 0x500
 
-/* Enqueues a one-CTA kernel whose pipeline wait can never complete: the wait gives up after
- * limit_us microseconds (at most 1e6), records MI_DEV_TIMEOUT_SELFTEST in the device error flag and
- * the kernel returns.  Exercises the failure path of the bounded waits without a fault or hang. */
+/* Enqueues a one-CTA kernel whose pipeline wait can never complete: the wait gives up after about
+ * limit_us microseconds (at most 1e6; the pipelines' own bounded wait, given as many polls as take
+ * that long), records MI_DEV_TIMEOUT_SELFTEST in the device error flag and the kernel returns.
+ * Exercises the failure path of the bounded waits without a fault or hang. */
 mi_status mi_selftest_wait_timeout(int limit_us, void* stream);
 
 /* ---------------------------------------------------------------------------------- block --- */
