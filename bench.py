@@ -665,13 +665,17 @@ def extras(mi, torch, devc, stream):
 L2_BYTES = 129e6  # GB300 L2
 
 
+# replays of each kernel's graph; the per-launch time is taken from the median replay
+KERNEL_REPLAYS = 5
+
+
 def kernel_times(mi, torch, g, inp, t, devc, reps, sampler=None):
     """Device time of each kernel of the block, launched alone at the workload's shapes through the
     single-kernel entry points.  Every kernel cycles through enough separate buffer sets (inputs,
     weights and outputs) that the bytes touched between two uses of one set are at least three
     times the 129 MB L2: each launch reads its operands from HBM, as the first use inside a forward
-    would, and pays for the write-back of earlier outputs.  Times are CUDA events around one replay
-    of a CUDA graph of those launches, divided by the launch count."""
+    would, and pays for the write-back of earlier outputs.  Times are CUDA events around each of a
+    few replays of a CUDA graph of those launches: the median replay, divided by the launch count."""
     R, H, I, nh, S, B = g.rows, g.hidden, g.mlp_inter, g.n_heads, g.seq, g.batch
     bf = torch.bfloat16
     w = inp.weights
@@ -750,13 +754,16 @@ def kernel_times(mi, torch, g, inp, t, devc, reps, sampler=None):
         torch.cuda.synchronize()
         gstream = torch.cuda.current_stream()
         t0 = time.time()
-        e0.record(gstream)
-        graph.replay()
-        e1.record(gstream)
-        torch.cuda.synchronize()
+        per_replay = []
+        for _ in range(KERNEL_REPLAYS):
+            e0.record(gstream)
+            graph.replay()
+            e1.record(gstream)
+            torch.cuda.synchronize()
+            per_replay.append(e0.elapsed_time(e1))
         t1 = time.time()
         launches = rounds * n_sets
-        ms = e0.elapsed_time(e1) / launches
+        ms = float(np.median(per_replay)) / launches
         del graph, sets
         ent = {"ms": ms}
         if "bytes" in work:
@@ -766,8 +773,9 @@ def kernel_times(mi, torch, g, inp, t, devc, reps, sampler=None):
             tf = work["flops"] / (ms * 1e-3) / 1e12
             ent.update(tflops=tf, frac_bf16_peak=tf / peaks["bf16_tflops"],
                        frac_bf16_nominal=tf / NOMINAL_PEAKS["bf16_tflops"])
-        ent["timing"] = (f"average over one CUDA graph of {launches} launches cycling through {n_sets} buffer sets "
-                         f"({n_sets * touched / 1e6:.0f} MB touched per cycle, L2 129 MB)")
+        ent["timing"] = (f"median over {KERNEL_REPLAYS} replays of one CUDA graph of {launches} launches cycling "
+                         f"through {n_sets} buffer sets ({n_sets * touched / 1e6:.0f} MB touched per cycle, "
+                         f"L2 129 MB), per launch")
         if sampler is not None:
             ck = sampler.summary(t0, t1)
             if ck:

@@ -92,13 +92,9 @@ __global__ void __launch_bounds__(kNormWarps * 32, 1)
     for (int k = 0; k < issued; ++k) issue(k);
   grid_dep_launch();
 
-  int k = 0;
-  for (; k < n_mine; ++k) {
-    const int sl = k % depth;
-    if (!mbar_wait_warp(&my_bars[sl], (uint32_t)((k / depth) & 1), &abort_flag, err, DEV_TIMEOUT_NORM + 1)) break;
-    const uint4* src = reinterpret_cast<const uint4*>(my_slots + (size_t)sl * kRowBytes);
-    const int row = r0 + warp + k * kNormWarps;
-    // sum of squares on packed pairs (f32x2): half the FMA instructions of a per-element chain
+  // Rows are taken two at a time when a warp has two left (they share one read of the modulation
+  // vectors), else one at a time.
+  auto row_rstd = [&](const uint4* src) {
     f32x2_t ss2 = 0ull;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
@@ -115,37 +111,60 @@ __global__ void __launch_bounds__(kNormWarps * 32, 1)
     float ss = ss_lo + ss_hi;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float rstd = rsqrtf(ss / (float)hidden + eps);
-    const int b = row / out_seq;
+    return rsqrtf(ss / (float)hidden + eps);
+  };
+  auto mod_piece = [&](uint4 v, uint4 vs, uint4 vc, f32x2_t rstd2) {
+    const f32x2_t one2 = f2_pack(1.0f, 1.0f);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w}, ws[4] = {vs.x, vs.y, vs.z, vs.w}, wc[4] = {vc.x, vc.y, vc.z, vc.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const f32x2_t t = f2_mul(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), rstd2);
+      const f32x2_t c = f2_add(f2_pack(bf16_lo(wc[e]), bf16_hi(wc[e])), one2);
+      float lo, hi;
+      f2_unpack(f2_fma(t, c, f2_pack(bf16_lo(ws[e]), bf16_hi(ws[e]))), lo, hi);
+      o[e] = pack_bf16x2(lo, hi);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  };
+  int k = 0;
+  while (k < n_mine) {
+    const int take = (depth >= 2 && k + 1 < n_mine && (r0 + warp + k * kNormWarps) / out_seq ==
+                                            (r0 + warp + (k + 1) * kNormWarps) / out_seq) ? 2 : 1;
+    const int slA = k % depth, slB = (k + 1) % depth;
+    if (!mbar_wait_warp(&my_bars[slA], (uint32_t)((k / depth) & 1), &abort_flag, err, DEV_TIMEOUT_NORM + 1)) break;
+    if (take == 2 &&
+        !mbar_wait_warp(&my_bars[slB], (uint32_t)(((k + 1) / depth) & 1), &abort_flag, err, DEV_TIMEOUT_NORM + 1))
+      break;
+    const uint4* srcA = reinterpret_cast<const uint4*>(my_slots + (size_t)slA * kRowBytes);
+    const uint4* srcB = reinterpret_cast<const uint4*>(my_slots + (size_t)slB * kRowBytes);
+    const int rowA = r0 + warp + k * kNormWarps;
+    const int rowB = rowA + kNormWarps;
+    const float rstdA = row_rstd(srcA);
+    const float rstdB = take == 2 ? row_rstd(srcB) : 0.0f;
+    const int b = rowA / out_seq;
     const uint4* sh = reinterpret_cast<const uint4*>(shift + (size_t)b * mod_bstride);
     const uint4* sc = reinterpret_cast<const uint4*>(scale + (size_t)b * mod_bstride);
-    uint4* orow = reinterpret_cast<uint4*>(out + (size_t)row * hidden);
-    const f32x2_t rstd2 = f2_pack(rstd, rstd);
-    const f32x2_t one2 = f2_pack(1.0f, 1.0f);
+    uint4* orowA = reinterpret_cast<uint4*>(out + (size_t)rowA * hidden);
+    uint4* orowB = reinterpret_cast<uint4*>(out + (size_t)rowB * hidden);
+    const f32x2_t rA = f2_pack(rstdA, rstdA), rB = f2_pack(rstdB, rstdB);
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {  // the row read again from its slot; (x * rstd) * (1 + scale) + shift
-      const uint4 v = src[i * 32 + lane];
+    for (int i = 0; i < NV; ++i) {  // each row read again from its slot; (x * rstd) * (1 + scale) + shift
       const uint4 vs = __ldg(sh + i * 32 + lane);
       const uint4 vc = __ldg(sc + i * 32 + lane);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w}, ws[4] = {vs.x, vs.y, vs.z, vs.w}, wc[4] = {vc.x, vc.y, vc.z, vc.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const f32x2_t t = f2_mul(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), rstd2);
-        const f32x2_t c = f2_add(f2_pack(bf16_lo(wc[e]), bf16_hi(wc[e])), one2);
-        float lo, hi;
-        f2_unpack(f2_fma(t, c, f2_pack(bf16_lo(ws[e]), bf16_hi(ws[e]))), lo, hi);
-        o[e] = pack_bf16x2(lo, hi);
-      }
-      orow[i * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+      orowA[i * 32 + lane] = mod_piece(srcA[i * 32 + lane], vs, vc, rA);
+      if (take == 2) orowB[i * 32 + lane] = mod_piece(srcB[i * 32 + lane], vs, vc, rB);
     }
-    __syncwarp();  // every lane is done with the slot before it is refilled
-    if (k + depth < n_mine) {
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        issue(k + depth);
+    __syncwarp();  // every lane is done with the slots before they are refilled
+    for (int t = 0; t < take; ++t) {
+      if (k + depth < n_mine) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          issue(k + depth);
+        }
+        ++issued;
       }
-      ++issued;
+      ++k;
     }
   }
   // after an abort: the copies still in flight land before the CTA's shared memory is released
