@@ -8,7 +8,8 @@
 // segments of one unit each, so no SM idles in a partial last wave.  A unit cut between two CTAs
 // is finished by whichever part arrives second: the first writes its unnormalised O, running max
 // and sum to scratch, the second adds both parts in a fixed order (keys from 0 first) and stores.
-// Without scratch (or with more units than fit the list), the grid is one CTA per unit.
+// Without scratch, or with more than 8 units per SM (where one CTA per unit balances better), the
+// grid is one CTA per unit.
 //   * warp 0   : TMA producer: the Q tiles of each segment, then K and V tiles of 128 keys into a
 //                2-stage ring (K and V with their own barriers so a K slot frees as soon as both
 //                score products have read it).  K comes from the packed [B, heads, S, 128] rows; V

@@ -335,8 +335,10 @@ mi_status mi_attention(const void* qp, const void* kp, const void* qkv, const ui
  * the (query-tile pair, key tile) steps, so no SM idles in a partial last wave.  A pair of query
  * tiles whose keys are split between two CTAs is finished by the second to arrive, which adds the
  * two partial results (unnormalised output, running max and sum) in a fixed order, so results
- * repeat bit for bit.  ws: at least mi_attention_workspace_size bytes, 256-byte aligned (0 bytes,
- * and ws may be NULL, when there are no more query-tile pairs than SMs).  Same page as above. */
+ * repeat bit for bit.  With no more query-tile pairs than SMs, or more than 8 per SM, the schedule
+ * is one CTA per pair, as in mi_attention.  ws: at least mi_attention_workspace_size bytes,
+ * 256-byte aligned (0 bytes, and ws may be NULL, when the schedule is one CTA per pair).  Same
+ * page as above. */
 mi_status mi_attention_workspace_size(int batch, int seq, int n_heads, size_t* bytes);
 mi_status mi_attention_ws(const void* qp, const void* kp, const void* qkv, const uint8_t* key_mask, void* o,
                           int batch, int seq, int n_heads, void* ws, size_t ws_bytes, void* stream);
