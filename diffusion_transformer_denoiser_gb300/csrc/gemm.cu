@@ -21,6 +21,8 @@
 // bit for bit, and runs the epilogue.  Nobody waits for another CTA: no co-residency is assumed.
 #include <stdlib.h>
 
+#include <climits>
+
 #include "mi_internal.h"
 #include "ptx.cuh"
 
@@ -563,7 +565,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Each CTA loads its own 128 rows of A and half of the 256-row W tile (64-column k-blocks), so a
 // pipeline stage holds 32 KB per CTA instead of 48 KB: six stages fit where the one-CTA kernel has
 // four, and each SM pulls a third less operand data per MMA.  The leader CTA (rank 0) issues the
-// MMAs for the pair; each CTA's epilogue drains its own 128 TMEM rows.
+// MMAs for the pair; each CTA's epilogue drains its own 128 TMEM rows.  A partial last wave of at
+// most half the clusters runs as half-width tiles (256 x 128, M=256 N=128 MMAs) on twice as many
+// clusters: each CTA still loads a 128-row W box, starting at its 64 rows, and the MMA reads the
+// first 64; an element's k-loop is the same in either width, so results do not change.
 //   * warp 0 of each CTA: TMA producer into its own ring.  Both CTAs' copies of a stage complete on
 //     the leader's `full` barrier (the pair form of the TMA), which the leader arms for both;
 //   * warp 1 of the leader: waits on `full`, issues the pair MMAs and commits to `empty` / `tfull`
@@ -636,10 +641,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   const int num_pm = (p.M + 2 * BM - 1) / (2 * BM);
   const int num_n = (EPI == EPI_SILU_GATE) ? (p.N / (BN / 2)) : (p.N + BN - 1) / BN;
-  const int num_units = num_pm * num_n;
+  const int num_tiles = num_pm * num_n;
+  // Tiles from p.half_from on (the partial last wave) run as two half-width tiles each (N = 128),
+  // so the last wave takes half a tile's time on twice as many clusters.
+  const int num_units = p.half_from < num_tiles ? num_tiles + (num_tiles - p.half_from) : num_tiles;
   const int kblocks = p.K / BK;
   const int cid = (int)blockIdx.x >> 1;
   const int n_clusters = (int)gridDim.x >> 1;
+  // unit u -> tile (pm, nb) and, for a half-width unit, which half (hh = 0, 1; -1 for a whole tile)
+  auto decode = [&](int u, int& pm, int& nb, int& hh) {
+    int t = u;
+    hh = -1;
+    if (u >= p.half_from) {
+      t = p.half_from + (u - p.half_from) / 2;
+      hh = (u - p.half_from) & 1;
+    }
+    pm = t % num_pm;
+    nb = t / num_pm;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -649,9 +668,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int u = cid; u < num_units && ok; u += n_clusters) {
-        const int pm = u % num_pm;
-        const int nb = u / num_pm;
+        int pm, nb, hh;
+        decode(u, pm, nb, hh);
         const int m0 = pm * 2 * BM + (int)rank * BM;
+        // W rows of this CTA's half of the unit's columns: 128 for a whole tile, 64 for a half tile
+        // (the 128-row box then brings 64 more, which the MMA does not read)
+        int b0;
+        if (EPI == EPI_SILU_GATE) {
+          // the leader loads gate rows, the follower the matching up rows
+          b0 = (int)rank * p.N + nb * (BN / 2) + (hh < 0 ? 0 : hh * 64);
+        } else {
+          b0 = hh < 0 ? nb * BN + (int)rank * 128 : nb * BN + hh * 128 + (int)rank * 64;
+        }
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait_noabort<true>(&empty[stage], phase ^ 1u, abort_flag, p.err, DEV_TIMEOUT_GEMM + 11)) {
             ok = false;
@@ -660,12 +688,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * L::STAGE_BYTES);
           const uint32_t fb = leader_full + stage * 8;
           tma_load_2d_pair(sA + stage * L::A_BYTES, &tmA, fb, kb * BK, m0);
-          if (EPI == EPI_SILU_GATE) {
-            // the leader loads the gate rows [nb*128, +128), the follower the up rows [N + nb*128, +128)
-            tma_load_2d_pair(sB + stage * L::B_BYTES, &tmB, fb, kb * BK, (int)rank * p.N + nb * (BN / 2));
-          } else {
-            tma_load_2d_pair(sB + stage * L::B_BYTES, &tmB, fb, kb * BK, nb * BN + (int)rank * 128);
-          }
+          tma_load_2d_pair(sB + stage * L::B_BYTES, &tmB, fb, kb * BK, b0);
           if (++stage == kPairStages) {
             stage = 0;
             phase ^= 1u;
@@ -682,7 +705,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (leader) {
       // ------------------------------------------------------------------ MMA issuer (leader)
-      constexpr uint32_t idesc = idesc_bf16(2 * BM, BN, false, false);
+      constexpr uint32_t idesc_full = idesc_bf16(2 * BM, BN, false, false);
+      constexpr uint32_t idesc_half = idesc_bf16(2 * BM, BN / 2, false, false);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -691,6 +715,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int u = cid; u < num_units && ok; u += n_clusters) {
         if (!mbar_wait_warp<true>(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, DEV_TIMEOUT_GEMM + 13)) break;
         tc_fence_after();
+        const uint32_t idesc = u < p.half_from ? idesc_full : idesc_half;
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait_warp<true>(&full[stage], phase, abort_flag, p.err, DEV_TIMEOUT_GEMM + 14)) {
@@ -729,8 +754,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cid; u < num_units; u += n_clusters) {
-      const int pm = u % num_pm;
-      const int nb = u / num_pm;
+      int pm, nb, hh;
+      decode(u, pm, nb, hh);
       const int row = pm * 2 * BM + (int)rank * BM + r_in_tile;
       const bool row_ok = row < p.M;
       if (EPI == EPI_GATED_RESIDUAL && row_ok) {
@@ -742,7 +767,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!mbar_wait_warp<true>(&tfull[acc], acc_phase, abort_flag, p.err, DEV_TIMEOUT_GEMM + 17)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      epilogue_tile<BN, EPI>(p, t_row, row, row_ok, nb);
+      if (hh < 0)
+        epilogue_tile<BN, EPI>(p, t_row, row, row_ok, nb);
+      else  // a half tile: column block 2 nb + hh of width 128
+        epilogue_tile<BN / 2, EPI>(p, t_row, row, row_ok, 2 * nb + hh);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(leader_tempty + acc * 8);
@@ -875,12 +903,18 @@ int pair_max_clusters(int num_sms) {
 }
 
 template <int EPI>
-cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int max_clusters,
+cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a_in, int max_clusters,
                              cudaStream_t s) {
+  GemmArgs a = a_in;
   const int num_pm = (a.M + 2 * BM - 1) / (2 * BM);
   const int num_n = (EPI == EPI_SILU_GATE) ? (a.N / 128) : (a.N + 255) / 256;
-  const int units = num_pm * num_n;
-  const int clusters = units < max_clusters ? units : max_clusters;
+  const int tiles = num_pm * num_n;
+  const int clusters = tiles < max_clusters ? tiles : max_clusters;
+  // a partial last wave of at most half the clusters runs as half-width tiles on twice as many
+  const int rem = tiles % clusters;
+  a.half_from = (tiles > clusters && rem > 0 && 2 * rem <= clusters && (EPI != EPI_SILU_GATE || a.N % 128 == 0))
+                    ? tiles - rem
+                    : INT_MAX;
   return launch_kernel(gemm_pair_kernel<EPI>, dim3(2 * clusters), dim3(kThreads), PairSmem::TOTAL, s, true, ta, tb,
                        a);
 }

@@ -49,6 +49,8 @@ struct GemmArgs {
   int* sk_count;               // [8 * SMs] arrival counters (one per 32-row quarter of a tail tile)
   float* sk_partial;           // [2 * SMs][256 columns][128 rows] fp32 partial tiles, two slots per CTA
   int sk_tiles;                // tiles on the stream-K tail (0: none)
+  int half_from;               // CTA-pair kernel: tiles from this index on run as two half-width tiles
+                               // each (set by the launcher)
 };
 
 cudaError_t gemm_launch(int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int num_sms,
