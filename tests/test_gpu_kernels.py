@@ -107,7 +107,9 @@ def test_gemm_rows_do_not_depend_on_the_launch():
     """A row's result does not depend on the launch it is computed in: 4130 rows in one launch (CTA
     pairs, the last 256-row pair tile holding 34 rows) give the bytes of two launches over rows
     0-4095 (CTA pairs, no ragged tile) and 4096-4129 (34 rows: the one-CTA kernel), and sampled
-    rows on both sides of the boundary match the oracle."""
+    rows on both sides of the boundary match the oracle.  Both pair launches end in a partial wave
+    that runs as half-width tiles (the last 24 of 1088 tiles, and the last 36 of 1024), on
+    different tiles, so the half-width tiles are checked against whole ones too."""
     mi = require_gpu()
     m, inter, k, top_rows = 4130, 8192, 3072, 4096
     rng = np.random.default_rng(4130)
